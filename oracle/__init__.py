@@ -1,0 +1,130 @@
+"""fp64 CPU oracle for split-KV flash attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's
+CPU-baseline / reference leg may import this package.  It shares no code with
+the CUDA path (split_kv_flash_gb300): the attention math lives in
+attn_oracle.c, the scheduling formulas in plan_oracle.py, both written from
+the pages' definitions.
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py and
+tests/test_plan_oracle.py (closed forms, invariances, library special cases and
+the pages' worked examples); none is "parity unpinned".
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        i32p = ctypes.POINTER(ctypes.c_int)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        L.oracle_attn_rows.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, i32p, ctypes.c_int, ctypes.c_double,
+                                       ctypes.c_int, ctypes.c_int, i32p, ctypes.c_long, f64p,
+                                       f64p, ctypes.c_int]
+        L.oracle_attn_rows.restype = ctypes.c_int
+        L.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, i32p, ctypes.c_int, ctypes.c_double,
+                                      ctypes.c_int, ctypes.c_int, f64p, f64p, ctypes.c_int]
+        L.oracle_attn_fwd.restype = ctypes.c_int
+        L.oracle_attn_fwd_split.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, i32p, f64p, f64p, ctypes.c_int]
+        L.oracle_attn_fwd_split.restype = ctypes.c_int
+        L.oracle_count_visible.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.oracle_count_visible.restype = ctypes.c_longlong
+        _lib = L
+    return _lib
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are raw bf16 bit patterns (uint16), got %s" % a.dtype)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def _i32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def _f64p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def attn_fwd(q, k, v, kv_len, scale, causal=False, window_left=-1, nthreads=0):
+    """Full fp64 attention.
+
+    q: uint16 bf16 bits [B, sq, Hq, d]; k, v: uint16 [sum(kv_len), Hkv, d].
+    Returns (out [B, sq, Hq, d] float64, lse [B, Hq, sq] float64).
+    """
+    B, sq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    kl, klp = _i32(kv_len)
+    out = np.zeros((B, sq, Hq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq, sq), dtype=np.float64)
+    rc = lib().oracle_attn_fwd(qp, kp, vp, B, Hq, Hkv, sq, klp, d, float(scale), int(causal),
+                               int(window_left), _f64p(out), _f64p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments")
+    return out, lse
+
+
+def attn_rows(q, k, v, kv_len, scale, rows, causal=False, window_left=-1, nthreads=0):
+    """Selected rows: rows is an int array [n, 3] of (b, h, i).
+    Returns (out [n, d] float64, lse [n] float64)."""
+    B, sq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    kl, klp = _i32(kv_len)
+    rows, rp = _i32(np.asarray(rows).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = lib().oracle_attn_rows(qp, kp, vp, B, Hq, Hkv, sq, klp, d, float(scale), int(causal),
+                                int(window_left), rp, n, _f64p(out), _f64p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_rows rejected its arguments")
+    return out, lse
+
+
+def attn_fwd_split(q, k, v, kv_len, scale, bounds, causal=False, window_left=-1, nthreads=0):
+    """Split reference: bounds int [B, S+1] key boundaries per sequence."""
+    B, sq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    bounds = np.asarray(bounds, dtype=np.int32).reshape(B, -1)
+    S = bounds.shape[1] - 1
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    kl, klp = _i32(kv_len)
+    bd, bdp = _i32(bounds)
+    out = np.zeros((B, sq, Hq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq, sq), dtype=np.float64)
+    rc = lib().oracle_attn_fwd_split(qp, kp, vp, B, Hq, Hkv, sq, klp, d, float(scale),
+                                     int(causal), int(window_left), S, bdp, _f64p(out),
+                                     _f64p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_split rejected its arguments")
+    return out, lse
+
+
+def count_visible(sq, sk, causal, window_left=-1):
+    return int(lib().oracle_count_visible(int(sq), int(sk), int(causal), int(window_left)))

@@ -1,0 +1,160 @@
+/*
+ * sk_attn.h -- C ABI of the split-KV flash attention forward library for
+ * GB300 (sm_103a).  Library: split_kv_flash_gb300/libskattn.so.
+ *
+ * Operation (what every entry point below computes or plans):
+ *   tiled attention forward with online softmax, parallelised over the KV axis
+ *   (flash-decoding).  For batch b, query head h and query row i:
+ *     O[b,i,h,:] = sum_j softmax_j(scale * <Q[b,i,h,:], K[off_b+j, h/G, :]>) V[off_b+j, h/G, :]
+ *     LSE[b,h,i] = ln sum_j exp(scale * <Q[b,i,h,:], K[off_b+j, h/G, :]>)
+ *   over the visible keys j of row i.
+ *   Sources: FlashAttention tiling strategy and scheduling chapter (分块策略与调度),
+ *   section 1 (tiling), section 3 (block-level masking skip), section 5 (split-K /
+ *   flash decoding with a separate combine step), section 6 (PackGQA); "The Occupancy
+ *   Awakening" (KV-split partial kernel plus reduction kernel); llama.cpp PR #21086
+ *   review (the stream-k fixup that merges partial tiles).
+ *
+ * Conventions shared by all entry points
+ *   - G = Hq / Hkv; query head h reads KV head h / G (contiguous groups).
+ *   - Q   [B, q_len, Hq, d]  bf16, row-major, device memory.
+ *   - K,V [sum_b kv_len[b], Hkv, d] bf16, row-major, device memory, packed by
+ *         sequence: sequence b starts at row off_b = kv_len[0] + ... + kv_len[b-1].
+ *         For equal lengths this is [B, kv_len, Hkv, d].
+ *   - O   [B, q_len, Hq, d]  bf16 output;  LSE [B, Hq, q_len] fp32 output (natural log).
+ *   - kv_len_host: HOST array of B non-negative lengths (read during the call only).
+ *   - causal != 0: query i sees keys j <= i + kv_len - q_len (bottom-right aligned,
+ *     tiling chapter section 3.1).  window_left >= 0: query i also needs
+ *     j >= i + kv_len - q_len - window_left (inclusive).  window_left < 0: no left
+ *     bound.  With causal == 0 a window bounds the left side only.
+ *   - A row with no visible key returns O = 0 and LSE = -inf.
+ *   - Supported: bf16 only, d in {64, 128}, Hq % Hkv == 0, q/k/v/out 16-byte
+ *     aligned, lse 4-byte aligned, workspace 256-byte aligned.  Anything else is
+ *     rejected with an error; there is no fallback path.
+ *   - Ownership: the caller owns every buffer.  The library allocates no device
+ *     memory and keeps no per-call state.  Inputs are never written.
+ *   - Errors are returned before any launch; no output is partly written by a
+ *     call that returns an error.  sk_attn_last_error() gives a one-line reason.
+ *   - Every K/V element that a kernel stages must be finite (the rows of the next
+ *     sequence that share a 128-row block with the end of a sequence are loaded
+ *     and then masked).
+ */
+#ifndef SK_ATTN_H
+#define SK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SK_OK = 0,
+    SK_ERR_INVALID_ARG = 1,          /* a size, pointer or flag is out of range */
+    SK_ERR_UNSUPPORTED = 2,          /* valid attention, but outside the supported domain */
+    SK_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < sk_attn_plan_info.workspace_bytes */
+    SK_ERR_MISALIGNED = 4,           /* a pointer violates the alignment rules above */
+    SK_ERR_CUDA = 5,                 /* a CUDA runtime/driver call failed */
+    SK_ERR_DEVICE_TIMEOUT = 6        /* a kernel gave up on a bounded wait (see sk_attn_workspace_status) */
+} sk_status;
+
+/* How the number of KV splits is chosen (sk_attn_opts.policy). */
+typedef enum {
+    SK_POLICY_DEFAULT = 0,      /* = SK_POLICY_FILL */
+    SK_POLICY_FILL = 1,         /* smallest per-CTA KV chunk such that all CTAs fit in one wave */
+    SK_POLICY_FA_HEURISTIC = 2, /* num_splits_heuristic, tiling chapter section 5.2 */
+    SK_POLICY_FIXED_CHUNK = 3,  /* clamp(ceil(kv_len / 2048), 1, 32), "The Occupancy Awakening" */
+    SK_POLICY_MIN_CHUNK = 4     /* 2 blocks per SM, each >= 256 keys, llama.cpp PR #21086 review */
+} sk_split_policy;
+
+/* Which kernel runs the partial (split) pass (sk_attn_opts.force_path / plan_info.path). */
+typedef enum {
+    SK_PATH_AUTO = 0,
+    SK_PATH_DECODE = 1,   /* <= 64 packed query rows per tile: KV rows on the MMA M axis */
+    SK_PATH_PREFILL = 2   /* 128 query rows per tile: query rows on the MMA M axis */
+} sk_path;
+
+/* Options; an all-zero struct (or NULL) selects the defaults. */
+typedef struct {
+    int policy;            /* sk_split_policy */
+    int force_num_splits;  /* > 0: exactly this many splits (clipped to the KV block count) */
+    int force_pack_gqa;    /* 0: should_pack_gqa heuristic; 1: pack; -1: do not pack */
+    int force_path;        /* sk_path */
+    int max_splits;        /* 0: 128 */
+    int num_sms;           /* 0: the current device's SM count; > 0: plan for this many SMs */
+    int debug_echo_plan;   /* 1: each CTA writes its KV block range into the workspace */
+    int wait_timeout_us;   /* 0: 2,000,000 us; bound on every device-side wait */
+    int debug_inject_stall;/* 1: one kernel wait targets a barrier nothing signals (tests the
+                              timeout path; the kernel reports SK_ERR_DEVICE_TIMEOUT) */
+    void* event_begin;     /* optional cudaEvent_t recorded just before the partial kernel */
+    void* event_end;       /* optional cudaEvent_t recorded just after it */
+} sk_attn_opts;
+
+/* The host scheduler's decisions for one problem. */
+typedef struct {
+    int path;                 /* sk_path actually used */
+    int kBlockM;              /* packed query rows per tile */
+    int kBlockN;              /* keys per KV block */
+    int pack_gqa;             /* 1: the G query heads of a KV head share one tile */
+    int head_tiles;           /* Hkv if pack_gqa else Hq */
+    int rows_per_head_tile;   /* q_len * G if pack_gqa else q_len */
+    int num_m_blocks;         /* ceil(rows_per_head_tile / kBlockM) */
+    int num_splits;           /* grid splits = max over sequences of the per-sequence count */
+    int num_splits_policy;    /* the count the policy chose before per-sequence sizing */
+    int num_n_blocks_max;     /* ceil(max kv_len / kBlockN) */
+    int grid_x, grid_y, grid_z; /* partial kernel grid: (num_m_blocks, head_tiles*num_splits, B) */
+    long long num_ctas;       /* grid_x * grid_y * grid_z */
+    int needs_combine;        /* 1: some sequence has more than one split */
+    size_t workspace_bytes;   /* bytes of device workspace sk_attn_fwd needs */
+    size_t echo_offset;       /* byte offset of the plan echo in the workspace */
+    size_t lse_part_offset;   /* byte offset of LSE partials [S][B][Hq][q_len] fp32 */
+    size_t o_part_offset;     /* byte offset of O partials [S][B][Hq][q_len][d] fp32 */
+} sk_attn_plan_info;
+
+/* Plan only (host, no device work).  Fills *info.  Same argument meaning as
+ * sk_attn_fwd.  With opts->num_sms > 0 it needs no GPU. */
+sk_status sk_attn_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
+                       int causal, int window_left, const sk_attn_opts* opts,
+                       sk_attn_plan_info* info);
+
+/* The host plan's KV block range of every CTA of the partial kernel, in launch
+ * order (x fastest, then y, then z): 4 int32 per CTA = {n_block_min, n_block_max,
+ * split word (low 16 bits split index, high 16 bits the sequence's split count),
+ * 1 if the CTA has work else 0}.  n_int32 must be >= 4 * num_ctas.  Tiling chapter
+ * sections 3.2 and 5.3. */
+sk_status sk_attn_plan_ranges(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
+                              int causal, int window_left, const sk_attn_opts* opts,
+                              int32_t* ranges_host, size_t n_int32);
+
+/* Attention forward.  Asynchronous on cuda_stream (a cudaStream_t; NULL = legacy
+ * default stream).  workspace: device buffer of >= info.workspace_bytes bytes,
+ * 256-byte aligned, zero-filled once before its first use (the library keeps
+ * its header valid afterwards); it may be reused by consecutive calls on the same
+ * stream.  Returns SK_OK once the kernels are enqueued. */
+sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
+                      float scale, int causal, int window_left,
+                      void* workspace, size_t ws_bytes, void* cuda_stream,
+                      const sk_attn_opts* opts);
+
+/* Copy n_int32 int32 of the plan echo (written when opts.debug_echo_plan = 1;
+ * same layout as sk_attn_plan_ranges) to host memory.  Synchronises cuda_stream. */
+sk_status sk_attn_read_plan_echo(const void* workspace, int32_t* ranges_host, size_t n_int32,
+                                 void* cuda_stream);
+
+/* Synchronise cuda_stream and read the workspace's device status word.  Returns
+ * SK_OK, or SK_ERR_DEVICE_TIMEOUT when a kernel gave up on a bounded wait since
+ * the last check (the word is then cleared).  *where (optional) receives the code
+ * of the wait that expired. */
+sk_status sk_attn_workspace_status(void* workspace, void* cuda_stream, int* where);
+
+const char* sk_attn_status_string(sk_status s);
+/* One-line reason for the last error returned on this thread ("" if none). */
+const char* sk_attn_last_error(void);
+/* Library ABI version: 100 * major + minor. */
+int sk_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SK_ATTN_H */

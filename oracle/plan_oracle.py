@@ -132,3 +132,66 @@ def split_counts(kv_lens, block_n: int, num_splits: int):
         return [1] * len(kv_lens)
     chunk = ceil_div(nmax, num_splits)
     return [max(1, ceil_div(n, chunk)) for n in nblk]
+
+
+# ----------------------------------------------------------------------------
+# Composition of the rules above into a per-CTA schedule, with the readings
+# that the pages leave open:
+#  * causal with a window is the local case with right window 0; a window
+#    without causal leaves the right side open (tiling chapter 3.2 code, where
+#    the right bound is n_idx + window_size_right for local);
+#  * total_mblocks = batch x (KV heads if packed else query heads) x m blocks
+#    (section 5.2 says batch x heads x m blocks; packing makes KV heads the heads);
+#  * max_splits = min(128, n blocks); the scan of section 5.2 runs 1..max_splits;
+#  * one grid (m blocks, head tiles x splits, batch), launch order x fastest,
+#    m block reversed for causal / local work (section 4.2 grid, section 4.4 LPT).
+
+WINDOW_RIGHT_OPEN = 1 << 30
+MAX_SPLITS = 128
+
+
+def mask_flags(causal: bool, window_left: int):
+    local = window_left >= 0
+    return (bool(causal) and not local, local, max(window_left, 0),
+            0 if causal else WINDOW_RIGHT_OPEN)
+
+
+def choose_splits(policy: str, B: int, head_tiles: int, num_m_blocks: int, kv_lens, d: int,
+                  block_n: int, num_sms: int, causal_or_local: bool, max_splits_opt: int = 128):
+    max_kv = max(kv_lens) if kv_lens else 0
+    nblk_max = ceil_div(max_kv, block_n)
+    max_splits = max(1, min(min(max_splits_opt, MAX_SPLITS), max(nblk_max, 1)))
+    tiles = B * head_tiles * num_m_blocks
+    if policy == "fa":
+        s = num_splits_heuristic(tiles, num_sms, nblk_max, num_m_blocks, max_kv * 2 * d * 2,
+                                 causal_or_local, max_splits)
+    elif policy == "fixed_chunk":
+        s = nsplit_fixed_chunk(max_kv)
+    elif policy == "min_chunk":
+        s = nsplit_min_chunk(num_sms, max(tiles, 1), max_kv)
+    else:
+        raise ValueError(policy)
+    return max(1, min(s, max_splits))
+
+
+def cta_table(sq: int, kv_lens, G: int, pack_gqa: bool, head_tiles: int, block_m: int,
+              block_n: int, num_m_blocks: int, num_splits_grid: int, splits_b, causal: bool,
+              window_left: int):
+    """Per-CTA (n_block_min, n_block_max, split word, has_work) in launch order."""
+    is_causal, local, wl, wr = mask_flags(causal, window_left)
+    reverse = bool(causal) or window_left >= 0
+    out = []
+    for b in range(len(kv_lens)):
+        for by in range(head_tiles * num_splits_grid):
+            split = by % num_splits_grid
+            for bx in range(num_m_blocks):
+                m_block = num_m_blocks - 1 - bx if reverse else bx
+                sb = splits_b[b]
+                word = (sb << 16) | split
+                if split >= sb:
+                    out.append((0, 0, word, 0))
+                    continue
+                lo, hi = n_block_min_max(sq, kv_lens[b], m_block, block_m, block_n, is_causal,
+                                         local, wl, wr, pack_gqa, G, split_word=word)
+                out.append((lo, hi, word, 1))
+    return out

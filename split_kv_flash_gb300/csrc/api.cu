@@ -1,0 +1,274 @@
+// api.cu -- the C ABI declared in include/sk_attn.h: argument checks, the host
+// plan, TMA tensor maps for K and V, and the launches of the partial kernel and
+// the combine kernel on the caller's stream.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <set>
+#include <string>
+#include <utility>
+
+#include "../../include/sk_attn.h"
+#include "fwd_common.cuh"
+#include "plan.h"
+
+namespace sk {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+sk_status fail(sk_status s, const std::string& msg) {
+    g_last_error = msg;
+    return s;
+}
+
+sk_status fail_cuda(cudaError_t e, const char* what) {
+    return fail(SK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// K or V as a 2-D bf16 tensor [rows][Hkv * d]; boxes of 128 rows x 64 columns
+// (128 bytes, the swizzle width), 128-byte swizzle, zero fill past the end.
+bool make_kv_map(CUtensorMap* m, const void* base, int Hkv, int d, long long rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cuuint64_t(Hkv) * cuuint64_t(d), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(Hkv) * cuuint64_t(d) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    int sms = 0, major = 0, minor = 0;
+};
+
+sk_status current_device(DeviceInfo* di) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && have[dev]) {
+        *di = cache[dev];
+        return SK_OK;
+    }
+    DeviceInfo d;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+        return fail_cuda(e, "cudaDeviceGetAttribute");
+    if (dev >= 0 && dev < 64) {
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *di = d;
+    return SK_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count({kernel, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({kernel, dev});
+    return e;
+}
+
+}  // namespace sk
+
+using namespace sk;
+
+extern "C" {
+
+sk_status sk_attn_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int causal,
+                       int window_left, const sk_attn_opts* opts, sk_attn_plan_info* info) {
+    g_last_error.clear();
+    if (!info) return fail(SK_ERR_INVALID_ARG, "info is NULL");
+    int sms = 0;
+    if (!opts || opts->num_sms <= 0) {
+        DeviceInfo di;
+        sk_status s = current_device(&di);
+        if (s != SK_OK) return s;
+        sms = di.sms;
+    }
+    Plan p;
+    std::string why;
+    sk_status s = make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, opts, sms, &p, &why);
+    if (s != SK_OK) return fail(s, why);
+    plan_to_info(p, info);
+    return SK_OK;
+}
+
+sk_status sk_attn_plan_ranges(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int causal,
+                              int window_left, const sk_attn_opts* opts, int32_t* ranges_host,
+                              size_t n_int32) {
+    g_last_error.clear();
+    if (!ranges_host) return fail(SK_ERR_INVALID_ARG, "ranges_host is NULL");
+    int sms = 0;
+    if (!opts || opts->num_sms <= 0) {
+        DeviceInfo di;
+        sk_status s = current_device(&di);
+        if (s != SK_OK) return s;
+        sms = di.sms;
+    }
+    Plan p;
+    std::string why;
+    sk_status s = make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, opts, sms, &p, &why);
+    if (s != SK_OK) return fail(s, why);
+    if (n_int32 < size_t(p.num_ctas) * 4) return fail(SK_ERR_INVALID_ARG, "ranges_host too small");
+    plan_ranges(p, ranges_host);
+    return SK_OK;
+}
+
+sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                      int Hkv, int q_len, const int* kv_len_host, int d, float scale, int causal,
+                      int window_left, void* workspace, size_t ws_bytes, void* cuda_stream,
+                      const sk_attn_opts* opts) {
+    g_last_error.clear();
+    sk_attn_opts o;
+    memset(&o, 0, sizeof o);
+    if (opts) o = *opts;
+    if (!(scale > 0.f) || !isfinite(scale)) return fail(SK_ERR_INVALID_ARG, "scale must be finite and > 0");
+    DeviceInfo di;
+    sk_status s = current_device(&di);
+    if (s != SK_OK) return s;
+    if (!(di.major == 10 && di.minor == 3))
+        return fail(SK_ERR_UNSUPPORTED, "this library runs on sm_103 (GB300) only");
+    Plan p;
+    std::string why;
+    s = make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, &o, di.sms, &p, &why);
+    if (s != SK_OK) return fail(s, why);
+    if (p.num_ctas == 0) return SK_OK;  // q_len == 0: nothing to compute
+    const long long total_kv = p.kv_off[size_t(B)];
+    if (!q || !out || !lse || !workspace) return fail(SK_ERR_INVALID_ARG, "NULL q, out, lse or workspace");
+    if (total_kv > 0 && (!k || !v)) return fail(SK_ERR_INVALID_ARG, "NULL k or v");
+    if (!aligned(q, 16) || !aligned(out, 16) || (total_kv > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+        return fail(SK_ERR_MISALIGNED, "q, k, v and out must be 16-byte aligned");
+    if (!aligned(lse, 4)) return fail(SK_ERR_MISALIGNED, "lse must be 4-byte aligned");
+    if (!aligned(workspace, 256)) return fail(SK_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    if (ws_bytes < p.ws_bytes) return fail(SK_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than plan.workspace_bytes");
+    if (total_kv >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "at most 2^31 - 1 KV rows in total");
+
+    // K/V tensor maps.  With no KV rows at all no tile is ever loaded; the map
+    // then points at `out` only so that it is well formed.
+    CUtensorMap tmK, tmV;
+    const void* kb = total_kv > 0 ? k : out;
+    const void* vb = total_kv > 0 ? v : out;
+    const long long rows = total_kv > 0 ? total_kv : 1;
+    if (!make_kv_map(&tmK, kb, Hkv, d, rows) || !make_kv_map(&tmV, vb, Hkv, d, rows))
+        return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    FwdParams fp;
+    memset(&fp, 0, sizeof fp);
+    fp.q = static_cast<const __nv_bfloat16*>(q);
+    fp.out = static_cast<__nv_bfloat16*>(out);
+    fp.lse = lse;
+    fp.o_part = reinterpret_cast<float*>(ws + p.o_off);
+    fp.lse_part = reinterpret_cast<float*>(ws + p.lse_off);
+    fp.echo = reinterpret_cast<int32_t*>(ws + p.echo_off);
+    fp.status = reinterpret_cast<uint32_t*>(ws);
+    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.G = p.G; fp.sq = q_len; fp.d = d;
+    fp.pack_gqa = p.pack_gqa ? 1 : 0;
+    fp.rows = p.rows;
+    fp.kBlockM = p.kBlockM; fp.kBlockN = p.kBlockN;
+    fp.num_m_blocks = p.num_m_blocks; fp.num_splits = p.num_splits; fp.head_tiles = p.head_tiles;
+    fp.flags = p.flags;
+    fp.causal = p.causal;
+    fp.window_left = p.window_left;
+    fp.scale_log2 = float(double(scale) * 1.4426950408889634074);
+    fp.reverse_m = p.reverse_m ? 1 : 0;
+    fp.echo_plan = o.debug_echo_plan ? 1 : 0;
+    fp.inject_stall = o.debug_inject_stall ? 1 : 0;
+    fp.timeout_ns = (unsigned long long)(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    cudaError_t e;
+    if (o.event_begin && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_begin), stream)) != cudaSuccess)
+        return fail_cuda(e, "cudaEventRecord");
+    e = (p.path == SK_PATH_DECODE) ? launch_decode(p, fp, tmK, tmV, stream)
+                                   : launch_prefill(p, fp, tmK, tmV, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "partial kernel launch");
+    if (o.event_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_end), stream)) != cudaSuccess)
+        return fail_cuda(e, "cudaEventRecord");
+    if (p.needs_combine) {
+        e = launch_combine(p, fp, stream);
+        if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
+    }
+    return SK_OK;
+}
+
+sk_status sk_attn_read_plan_echo(const void* workspace, int32_t* ranges_host, size_t n_int32, void* cuda_stream) {
+    g_last_error.clear();
+    if (!workspace || !ranges_host) return fail(SK_ERR_INVALID_ARG, "NULL pointer");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(ranges_host, static_cast<const uint8_t*>(workspace) + 256, n_int32 * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpy");
+    return SK_OK;
+}
+
+sk_status sk_attn_workspace_status(void* workspace, void* cuda_stream, int* where) {
+    g_last_error.clear();
+    if (where) *where = 0;
+    if (!workspace) return fail(SK_ERR_INVALID_ARG, "NULL workspace");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, workspace, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpy");
+    if (word == 0) return SK_OK;
+    if (where) *where = int(word);
+    e = cudaMemset(workspace, 0, 4);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemset");
+    return fail(SK_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait (code " + std::to_string(word) + ")");
+}
+
+const char* sk_attn_status_string(sk_status s) {
+    switch (s) {
+        case SK_OK: return "SK_OK";
+        case SK_ERR_INVALID_ARG: return "SK_ERR_INVALID_ARG";
+        case SK_ERR_UNSUPPORTED: return "SK_ERR_UNSUPPORTED";
+        case SK_ERR_WORKSPACE_TOO_SMALL: return "SK_ERR_WORKSPACE_TOO_SMALL";
+        case SK_ERR_MISALIGNED: return "SK_ERR_MISALIGNED";
+        case SK_ERR_CUDA: return "SK_ERR_CUDA";
+        case SK_ERR_DEVICE_TIMEOUT: return "SK_ERR_DEVICE_TIMEOUT";
+    }
+    return "SK_ERR_UNKNOWN";
+}
+
+const char* sk_attn_last_error(void) { return g_last_error.c_str(); }
+
+int sk_attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// fwd_common.cuh -- parameters shared by the partial (split) kernels and the
+// combine kernel, and the launch entry points implemented in the .cu files.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "block_range.h"
+#include "plan.h"
+
+namespace sk {
+
+// Status-word codes: (kernel << 8) | wait site.
+enum : uint32_t {
+    kKernDecode = 1,
+    kKernPrefill = 2,
+    kSiteProducerEmpty = 1,
+    kSiteMmaQ = 2,
+    kSiteMmaFull = 3,
+    kSiteMmaSEmpty = 4,
+    kSiteMmaPFull = 5,
+    kSiteSoftmaxSFull = 6,
+    kSiteSoftmaxODone = 7,
+    kSiteInjected = 8,
+};
+
+struct FwdParams {
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    float* lse;
+    float* o_part;     // [S][B][Hq][sq][d]
+    float* lse_part;   // [S][B][Hq][sq]
+    int32_t* echo;     // 4 int32 per CTA
+    uint32_t* status;  // workspace header word
+    int B, Hq, Hkv, G, sq, d;
+    int pack_gqa;
+    int rows;          // packed rows per head tile
+    int kBlockM, kBlockN, num_m_blocks, num_splits, head_tiles;
+    MaskFlags flags;   // block-level flags
+    int causal;        // element-level mask
+    int window_left;   // < 0: none
+    float scale_log2;  // softmax scale * log2(e)
+    int reverse_m;
+    int echo_plan;
+    int inject_stall;
+    unsigned long long timeout_ns;
+};
+
+// Per-sequence lengths, offsets and split counts.  Equal lengths need no table.
+struct UniformSeqs {
+    int len;
+    int splits;
+    __device__ __forceinline__ int seq_len(int) const { return len; }
+    __device__ __forceinline__ int seq_off(int b) const { return b * len; }
+    __device__ __forceinline__ int splits_of(int) const { return splits; }
+};
+
+struct VarlenSeqs {
+    int off[kMaxVarlenBatch + 1];
+    unsigned short splits[kMaxVarlenBatch];
+    __device__ __forceinline__ int seq_len(int b) const { return off[b + 1] - off[b]; }
+    __device__ __forceinline__ int seq_off(int b) const { return off[b]; }
+    __device__ __forceinline__ int splits_of(int b) const { return splits[b]; }
+};
+
+// Packed row r of head tile ht -> (query position i, query head h).
+// Tiling chapter section 6.1/6.3: with PackGQA the G query heads of KV head ht
+// share the tile, row r = i * G + g.
+struct RowMap {
+    int i, h;
+};
+__device__ __forceinline__ RowMap map_row(const FwdParams& p, int ht, int r) {
+    RowMap m;
+    if (p.pack_gqa) {
+        m.i = r / p.G;
+        m.h = ht * p.G + (r - m.i * p.G);
+    } else {
+        m.i = r;
+        m.h = ht;
+    }
+    return m;
+}
+
+// Launchers (return a CUDA error code).
+cudaError_t launch_decode(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, cudaStream_t stream);
+cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, cudaStream_t stream);
+cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream);
+
+void fill_varlen(const Plan& plan, VarlenSeqs* v);
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+}  // namespace sk

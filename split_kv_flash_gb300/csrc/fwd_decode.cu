@@ -1,0 +1,474 @@
+// fwd_decode.cu -- split-KV partial kernel for tiles of at most 64 packed query
+// rows (decode, speculative verify, GQA decode), sm_103a.
+//
+// One CTA owns (KV head tile, split, sequence).  The KV block range comes from
+// the block-range rules of the FlashAttention tiling chapter (section 3.2: causal /
+// local bounds; section 5.3: the split's share of the range).  Because the query
+// side is small, the MMAs put the 128 KV rows of a block on the tensor-core M
+// axis and the packed query rows on N ("swap AB"):
+//   S^T[128 keys x NP] = K_blk[128 x d] . Q^T              (tcgen05, TMEM)
+//   O^T[d x NP]       += V_blk^T[d x 128] . P^T[128 x NP]   (tcgen05, TMEM)
+// Online softmax (running max m, running sum l, fp32 accumulator) follows the
+// flash-decode description of "The Occupancy Awakening"; each split writes its
+// normalised partial O and log-sum-exp for the combine kernel, or the final
+// output when the sequence has a single split.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads of K/V blocks into a
+// multi-stage shared-memory ring; warp 1 owns TMEM and issues the MMAs; warps
+// 2-5 (128 threads, thread t <-> TMEM lane t = key t of S^T and d-row t of O^T)
+// do the softmax, the rescaling and the epilogue.
+#include <math.h>
+
+#include "fwd_common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace sk {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int HD, int NP>
+struct DecodeCfg {
+    static constexpr int kStages = HD == 128 ? (NP <= 32 ? 3 : 2) : 4;
+    static constexpr int kKBytes = 128 * HD * 2;      // K block: 128 rows x HD
+    static constexpr int kVBytes = 128 * 128 * 2;     // V block region: 128 rows x 128 (M = 128 for PV)
+    static constexpr int kVLoadBytes = 128 * HD * 2;  // bytes actually loaded
+    static constexpr int kStageBytes = kKBytes + kVBytes;
+    static constexpr int kQBytes = NP * HD * 2;
+    static constexpr int kPBytes = NP * 128 * 2;
+    static constexpr int kOffStages = 0;
+    static constexpr int kOffQ = kStages * kStageBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;
+    static constexpr int kOffRed = kOffP + kPBytes;            // float red[4][NP]
+    static constexpr int kOffM = kOffRed + 4 * NP * 4;         // float m[NP]
+    static constexpr int kOffAlpha = kOffM + NP * 4;           // float alpha[NP]
+    static constexpr int kOffL = kOffAlpha + NP * 4;           // float l[NP]
+    static constexpr int kOffDiag = kOffL + NP * 4;            // int diag[NP]
+    static constexpr int kOffBars = (kOffDiag + NP * 4 + 7) / 8 * 8;
+    static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1 + 1 + 1;
+    static constexpr int kOffMisc = kOffBars + kNumBars * 8;   // tmem base, abort flag
+    static constexpr int kSmemBytes = kOffMisc + 16;
+    static constexpr int kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1024
+    static constexpr int kTmemCols = (3 * NP <= 32) ? 32 : (3 * NP <= 64) ? 64 : (3 * NP <= 128) ? 128 : 256;
+    static_assert(kSmemAlloc <= 232448, "shared memory budget");
+    static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "UMMA operands need 1024-byte alignment");
+};
+
+template <int HD, int NP, class Seqs>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_decode_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Seqs seqs) {
+    using C = DecodeCfg<HD, NP>;
+    constexpr int ST = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- which tile
+    const TileCoord tc = tile_of_cta(blockIdx.x, blockIdx.y, blockIdx.z, p.num_m_blocks, p.num_splits,
+                                     p.reverse_m != 0);
+    const int b = tc.batch;
+    const int ht = tc.head_tile;
+    const int sb = seqs.splits_of(b);
+    const uint32_t word = split_word(tc.split, sb);
+    const long long cta_lin =
+        blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+    if (tc.split >= sb) {
+        if (p.echo_plan && threadIdx.x == 0) {
+            int4 e = make_int4(0, 0, int(word), 0);
+            *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = e;
+        }
+        return;
+    }
+    const int sk = seqs.seq_len(b);
+    const int kv_off = seqs.seq_off(b);
+    const BlockRange br =
+        n_block_range(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.flags, p.pack_gqa != 0, p.G, word);
+    const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
+    if (p.echo_plan && threadIdx.x == 0) {
+        int4 e = make_int4(br.lo, br.hi, int(word), 1);
+        *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = e;
+    }
+    const int m0 = tc.m_block * p.kBlockM;
+    const int rows_valid = min(p.kBlockM, p.rows - m0);
+
+    // ---- shared memory carve-up
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + C::kOffQ;
+    const uint32_t sP = sbase + C::kOffP;
+    float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+    float* sm_m = reinterpret_cast<float*>(smem + C::kOffM);
+    float* sm_alpha = reinterpret_cast<float*>(smem + C::kOffAlpha);
+    float* sm_l = reinterpret_cast<float*>(smem + C::kOffL);
+    int* sm_diag = reinterpret_cast<int*>(smem + C::kOffDiag);
+    const uint32_t bars = sbase + C::kOffBars;
+    auto bar_full = [&](int s) { return bars + 8u * s; };
+    auto bar_empty = [&](int s) { return bars + 8u * (ST + s); };
+    auto bar_sfull = [&](int i) { return bars + 8u * (2 * ST + i); };
+    auto bar_sempty = [&](int i) { return bars + 8u * (2 * ST + 2 + i); };
+    const uint32_t bar_pfull = bars + 8u * (2 * ST + 4);
+    const uint32_t bar_odone = bars + 8u * (2 * ST + 5);
+    const uint32_t bar_qfull = bars + 8u * (2 * ST + 6);
+    const uint32_t bar_never = bars + 8u * (2 * ST + 7);
+    const uint32_t bar_drain = bars + 8u * (2 * ST + 8);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    auto stage_k = [&](int s) { return sbase + C::kOffStages + uint32_t(s) * C::kStageBytes; };
+    auto stage_v = [&](int s) { return stage_k(s) + C::kKBytes; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_sfull(i), 1);
+            mbar_init(bar_sempty(i), 128);
+        }
+        mbar_init(bar_pfull, 128);
+        mbar_init(bar_odone, 1);
+        mbar_init(bar_qfull, 128);
+        mbar_init(bar_never, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t tS0 = tmem;           // S^T buffers: columns [0, NP), [NP, 2NP)
+    const uint32_t tO = tmem + 2 * NP;   // O^T: columns [2NP, 3NP)
+    WaitCtl wc{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ===================== TMA producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int j = 0; j < nblocks; ++j) {
+                const int s = j % ST;
+                const int u = j / ST;
+                if (u >= 1 && !mbar_wait(bar_empty(s), (u - 1) & 1, wc, (kKernDecode << 8) | kSiteProducerEmpty))
+                    break;
+                mbar_arrive_expect_tx(bar_full(s), 2 * C::kVLoadBytes);
+                const int y = kv_off + (br.lo + j) * 128;
+                const int kvh = p.pack_gqa ? ht : ht / p.G;
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c) {
+                    tma_load_2d(stage_k(s) + c * 16384, &tmK, bar_full(s), kvh * HD + c * 64, y, pol);
+                    tma_load_2d(stage_v(s) + c * 16384, &tmV, bar_full(s), kvh * HD + c * 64, y, pol);
+                }
+                issued = j + 1;
+            }
+            // Drain: the last load of every stage must land before the CTA exits.
+            for (int j = issued - 1; j >= 0 && j >= issued - ST; --j)
+                mbar_drain(bar_full(j % ST), (j / ST) & 1, p.timeout_ns);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = make_idesc_bf16(128, NP, false, false);
+            constexpr uint32_t idesc_pv = make_idesc_bf16(128, NP, true, false);
+            bool ok = true;
+            if (p.inject_stall)
+                ok = mbar_wait(bar_never, 0, wc, (kKernDecode << 8) | kSiteInjected);
+            if (nblocks > 0)
+                ok = mbar_wait(bar_qfull, 0, wc, (kKernDecode << 8) | kSiteMmaQ) && ok;
+            auto issue_pv = [&](int jj) {
+                bool good = mbar_wait(bar_pfull, jj & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
+                tc_fence_after();
+                if (good) {
+                    const int s = jj % ST;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t a = make_sdesc_sw128(stage_v(s) + kk * 2048, 16384, 1024);
+                        const uint64_t bd = make_sdesc_sw128(sP + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
+                        umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar_odone);
+                    umma_commit(bar_empty(s));
+                }
+            };
+            for (int j = 0; j < nblocks; ++j) {
+                const int s = j % ST;
+                bool good = mbar_wait(bar_full(s), (j / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
+                if (j >= 2)
+                    good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
+                                     (kKernDecode << 8) | kSiteMmaSEmpty) && good;
+                tc_fence_after();
+                if (good && ok) {
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint64_t a = make_sdesc_sw128(stage_k(s) + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = make_sdesc_sw128(sQ + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
+                        umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar_sfull(j & 1));
+                }
+                if (j >= 1) issue_pv(j - 1);
+            }
+            if (nblocks >= 1) issue_pv(nblocks - 1);
+            // Every issued MMA completes before TMEM is released.
+            umma_commit(bar_drain);
+            mbar_drain(bar_drain, 0, p.timeout_ns);
+        }
+    } else {
+        // ===================== softmax / correction / epilogue (128 threads)
+        const int sidx = threadIdx.x - 64;            // 0..127 for cooperative loops
+        const int kt = 32 * (warp & 3) + lane;        // TMEM lane owned by this thread
+        const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+        const int diag_shift = sk - p.sq;
+
+        // Q tile -> smem (K-major, 128B swizzle), padded rows zero.
+        constexpr int kGran = HD / 8;  // 16-byte granules per row
+        for (int idx = sidx; idx < NP * kGran; idx += 128) {
+            const int r = idx / kGran;
+            const int g16 = idx - r * kGran;
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (r < rows_valid) {
+                const RowMap rm = map_row(p, ht, m0 + r);
+                val = __ldg(reinterpret_cast<const uint4*>(
+                    p.q + ((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + g16 * 8));
+            }
+            const uint32_t dst = sQ + (g16 >> 3) * (NP * 128) + sw128_offset(r, g16 & 7);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val.x), "r"(val.y),
+                         "r"(val.z), "r"(val.w)
+                         : "memory");
+        }
+        if (sidx < NP) {
+            sm_m[sidx] = -INFINITY;
+            sm_diag[sidx] = (sidx < rows_valid) ? map_row(p, ht, m0 + sidx).i + diag_shift : 0;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar_qfull);
+        named_bar_sync(1, 128);
+
+        // Rows whose query sees the whole block need no element mask.
+        const int diag_lo = (rows_valid > 0) ? sm_diag[0] : 0;
+        const int diag_hi = (rows_valid > 0) ? sm_diag[rows_valid - 1] : 0;
+        const bool has_causal = p.causal != 0;
+        const bool has_window = p.window_left >= 0;
+
+        float l_t[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) l_t[q] = 0.f;
+
+        for (int j = 0; j < nblocks; ++j) {
+            const int n = br.lo + j;
+            float x[NP];
+            mbar_wait(bar_sfull(j & 1), (j >> 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxSFull);
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < NP / 16; ++c) tmem_ld16(tS0 + (j & 1) * NP + lane_off + c * 16, x + c * 16);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar_sempty(j & 1));
+
+            const int key = n * 128 + kt;
+            const int blk_first = n * 128, blk_last = n * 128 + 127;
+            const bool need_mask = (blk_last >= sk) || (has_causal && blk_last > diag_lo) ||
+                                   (has_window && blk_first < diag_hi - p.window_left);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                float v = x[q] * p.scale_log2;
+                if (q >= rows_valid) v = -INFINITY;
+                if (need_mask) {
+                    const int dg = sm_diag[q];
+                    if (key >= sk || (has_causal && key > dg) || (has_window && key < dg - p.window_left))
+                        v = -INFINITY;
+                }
+                x[q] = v;
+            }
+            bool need = false;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) need |= x[q] > sm_m[q] + kRescaleThreshold;
+            const bool need_all = named_bar_or(1, 128, need);
+            if (need_all) {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const float v = warp_max(x[q]);
+                    if (lane == 0) red[(warp & 3) * NP + q] = v;
+                }
+                named_bar_sync(1, 128);
+                if (sidx < NP) {
+                    const int q = sidx;
+                    const float bm = fmaxf(fmaxf(red[q], red[NP + q]), fmaxf(red[2 * NP + q], red[3 * NP + q]));
+                    const float mo = sm_m[q];
+                    const float mn = fmaxf(mo, bm);
+                    sm_alpha[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+                    sm_m[q] = mn;
+                }
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) l_t[q] *= sm_alpha[q];
+            }
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float mq = sm_m[q];
+                const float pv = (mq == -INFINITY) ? 0.f : fast_exp2(x[q] - mq);
+                l_t[q] += pv;
+                x[q] = pv;
+            }
+            // PV of the previous block must be done before P and O are touched.
+            if (j >= 1) {
+                mbar_wait(bar_odone, (j - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+                tc_fence_after();
+                if (need_all) {
+#pragma unroll
+                    for (int c = 0; c < NP / 16; ++c) {
+                        float o[16];
+                        tmem_ld16(tO + lane_off + c * 16, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
+                        tmem_st16(tO + lane_off + c * 16, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P^T[q][kt] (bf16) -> smem, K-major over keys, 128B swizzle.
+            {
+                const uint32_t base = sP + (kt >> 6) * (NP * 128);
+                const int g = (kt & 63) >> 3;
+                const uint32_t within = (kt & 7) * 2;
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const __nv_bfloat16 hv = __float2bfloat16_rn(x[q]);
+                    const uint16_t bits = *reinterpret_cast<const uint16_t*>(&hv);
+                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(base + sw128_offset(q, g) + within),
+                                 "h"(bits)
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_pfull);
+        }
+
+        // ---- epilogue: l across the 128 key lanes, then O^T / l
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const float v = warp_sum(l_t[q]);
+            if (lane == 0) red[(warp & 3) * NP + q] = v;
+        }
+        named_bar_sync(1, 128);
+        if (sidx < NP) sm_l[sidx] = red[sidx] + red[NP + sidx] + red[2 * NP + sidx] + red[3 * NP + sidx];
+        named_bar_sync(1, 128);
+
+        float o[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) o[q] = 0.f;
+        if (nblocks >= 1) {
+            mbar_wait(bar_odone, (nblocks - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < NP / 16; ++c) tmem_ld16(tO + lane_off + c * 16, o + c * 16);
+            tmem_wait_ld();
+        }
+        const bool final_out = (sb == 1);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            if (q < rows_valid) {
+                const RowMap rm = map_row(p, ht, m0 + q);
+                const float l = sm_l[q];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float val = l > 0.f ? o[q] * inv : 0.f;
+                const float lse = l > 0.f ? (sm_m[q] + log2f(l)) * kLn2 : -INFINITY;
+                if (final_out) {
+                    if (kt < HD)
+                        p.out[((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + kt] = __float2bfloat16_rn(val);
+                    if (kt == 0) p.lse[(size_t(b) * p.Hq + rm.h) * p.sq + rm.i] = lse;
+                } else {
+                    const size_t prow = ((size_t(tc.split) * p.B + b) * p.Hq + rm.h) * p.sq + rm.i;
+                    if (kt < HD) p.o_part[prow * HD + kt] = val;
+                    if (kt == 0) p.lse_part[prow] = lse;
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int HD, int NP, class Seqs>
+cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
+                       const CUtensorMap& tmV, const Seqs& seqs, cudaStream_t stream) {
+    using C = DecodeCfg<HD, NP>;
+    auto kern = fwd_decode_kernel<HD, NP, Seqs>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
+    kern<<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tmK, tmV, seqs);
+    return cudaGetLastError();
+}
+
+template <int HD, class Seqs>
+cudaError_t dispatch_np(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
+                        const CUtensorMap& tmV, const Seqs& seqs, cudaStream_t stream) {
+    switch (plan.kBlockM) {
+        case 16: return launch_one<HD, 16>(plan, p, tmK, tmV, seqs, stream);
+        case 32: return launch_one<HD, 32>(plan, p, tmK, tmV, seqs, stream);
+        case 48: return launch_one<HD, 48>(plan, p, tmK, tmV, seqs, stream);
+        case 64: return launch_one<HD, 64>(plan, p, tmK, tmV, seqs, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+void fill_varlen(const Plan& plan, VarlenSeqs* v) {
+    for (int b = 0; b <= plan.B && b <= kMaxVarlenBatch; ++b) v->off[b] = int(plan.kv_off[size_t(b)]);
+    for (int b = 0; b < plan.B && b < kMaxVarlenBatch; ++b)
+        v->splits[b] = (unsigned short)plan.splits_b[size_t(b)];
+}
+
+cudaError_t launch_decode(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, cudaStream_t stream) {
+    if (!plan.varlen) {
+        UniformSeqs u{plan.kv_len[0], plan.splits_b[0]};
+        return plan.d == 128 ? dispatch_np<128>(plan, p, tmK, tmV, u, stream)
+                             : dispatch_np<64>(plan, p, tmK, tmV, u, stream);
+    }
+    VarlenSeqs v;  // copied into the launch's parameter buffer at launch
+    fill_varlen(plan, &v);
+    return plan.d == 128 ? dispatch_np<128>(plan, p, tmK, tmV, v, stream)
+                         : dispatch_np<64>(plan, p, tmK, tmV, v, stream);
+}
+
+}  // namespace sk

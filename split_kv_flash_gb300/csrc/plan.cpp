@@ -1,0 +1,278 @@
+// plan.cpp -- host scheduler: path and tile choice, GQA packing, split count,
+// per-sequence split counts, grid and workspace layout.  Pure C++; a plan for an
+// explicit SM count needs no GPU.
+#include "plan.h"
+
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
+namespace sk {
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// FlashAttention tiling chapter, section 5.2: "KV head > L2 (50MB)" branch.
+constexpr long long kL2SplitBytes = 50LL * 1024 * 1024;
+
+}  // namespace
+
+// Tiling chapter section 6.2 (should_pack_gqa): efficiency = useful rows / rows
+// rounded up to block_m; pack when the unpacked efficiency is below 0.9 of the
+// packed one.  float ratios against a double constant, as printed.
+bool should_pack_gqa(bool varlen_q, int seqlen_q, int qhead_per_khead, int block_m) {
+    if (varlen_q) return true;
+    auto round_up = [](int a, int b) { return (a + b - 1) / b * b; };
+    const float nopack = float(seqlen_q) / float(round_up(seqlen_q, block_m));
+    const int packed = seqlen_q * qhead_per_khead;
+    const float pack = float(packed) / float(round_up(packed, block_m));
+    return nopack < 0.9 * pack;
+}
+
+// Tiling chapter section 5.2 (num_splits_heuristic): fill gate at 0.8 * SMs,
+// L2 branch, short-K shortcut, then the smallest split count whose wave
+// efficiency reaches 0.85 of the best one.
+int num_splits_fa_heuristic(int total_mblocks, int num_sms, int num_n_blocks, int num_m_blocks,
+                            long long size_one_kv_head, bool is_causal_or_local, int max_splits) {
+    if (total_mblocks >= 0.8 * num_sms) {
+        if (size_one_kv_head > kL2SplitBytes && num_m_blocks >= 2 * num_sms && !is_causal_or_local)
+            return int(std::min<long long>((size_one_kv_head + kL2SplitBytes - 1) / kL2SplitBytes,
+                                           (long long)max_splits));
+        return 1;
+    }
+    if (num_n_blocks <= 4) return 1;
+    std::vector<float> eff(size_t(std::max(max_splits, 0)));
+    float best = 0.f;
+    for (int s = 1; s <= max_splits; ++s) {
+        const float waves = float(total_mblocks * s) / float(num_sms);
+        const float e = waves / ceilf(waves);
+        eff[size_t(s - 1)] = e;
+        if (e > best) best = e;
+    }
+    for (int s = 1; s <= max_splits; ++s)
+        if (eff[size_t(s - 1)] >= 0.85 * best) return s;
+    return 1;
+}
+
+// Per-sequence split counts: one chunk ceil(n_blocks_max / S) for the batch,
+// each sequence takes the chunks it needs (high 16 bits of the split word).
+std::vector<int> per_sequence_splits(const std::vector<int>& kv_len, int block_n, int num_splits) {
+    std::vector<int> out(kv_len.size(), 1);
+    int nmax = 0;
+    for (int s : kv_len) nmax = std::max(nmax, ceil_div_c(s, block_n));
+    if (num_splits <= 1 || nmax == 0) return out;
+    const int chunk = ceil_div_c(nmax, num_splits);
+    for (size_t b = 0; b < kv_len.size(); ++b)
+        out[b] = std::max(1, ceil_div_c(ceil_div_c(kv_len[b], block_n), chunk));
+    return out;
+}
+
+namespace {
+
+// SK_POLICY_FILL: the smallest per-CTA chunk (in KV blocks) for which every CTA
+// of the partial kernel fits in one wave of `capacity` CTAs.  Returns S.
+int fill_policy(const Plan& p, int capacity, int max_splits) {
+    const long long tiles = (long long)p.B * p.head_tiles * p.num_m_blocks;
+    if (tiles >= capacity || p.nblk_max <= 1) return 1;
+    int best = 1;
+    // S candidates from large to small; the first whose per-sequence counts
+    // fit in one wave wins (larger S = smaller chunk per CTA).
+    const int smax = std::min(max_splits, p.nblk_max);
+    for (int S = smax; S >= 1; --S) {
+        const std::vector<int> sb = per_sequence_splits(p.kv_len, p.kBlockN, S);
+        long long ctas = 0;
+        for (int c : sb) ctas += (long long)c * p.head_tiles * p.num_m_blocks;
+        if (ctas <= capacity) { best = S; break; }
+    }
+    // drop splits that would only repeat the same chunk size
+    const int chunk = ceil_div_c(p.nblk_max, best);
+    return ceil_div_c(p.nblk_max, chunk);
+}
+
+}  // namespace
+
+sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int causal,
+                    int window_left, const sk_attn_opts* opts_in, int device_num_sms, Plan* out,
+                    std::string* why) {
+    sk_attn_opts opts;
+    memset(&opts, 0, sizeof opts);
+    if (opts_in) opts = *opts_in;
+    Plan p;
+    auto fail = [&](sk_status s, const char* msg) {
+        if (why) *why = msg;
+        return s;
+    };
+    if (B <= 0 || B > 65535) return fail(SK_ERR_INVALID_ARG, "B must be in [1, 65535]");
+    if (Hq <= 0 || Hkv <= 0) return fail(SK_ERR_INVALID_ARG, "head counts must be positive");
+    if (Hq % Hkv != 0) return fail(SK_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+    if (q_len < 0 || q_len > kMaxSeqLen) return fail(SK_ERR_INVALID_ARG, "q_len out of range");
+    if (!kv_len_host) return fail(SK_ERR_INVALID_ARG, "kv_len_host is NULL");
+    if (d != 64 && d != 128) return fail(SK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (opts.policy < 0 || opts.policy > SK_POLICY_MIN_CHUNK)
+        return fail(SK_ERR_INVALID_ARG, "unknown split policy");
+    if (opts.force_path < 0 || opts.force_path > SK_PATH_PREFILL)
+        return fail(SK_ERR_INVALID_ARG, "unknown path");
+    if (opts.force_pack_gqa < -1 || opts.force_pack_gqa > 1)
+        return fail(SK_ERR_INVALID_ARG, "force_pack_gqa must be -1, 0 or 1");
+    if (opts.max_splits < 0 || opts.force_num_splits < 0 || opts.num_sms < 0 ||
+        opts.wait_timeout_us < 0)
+        return fail(SK_ERR_INVALID_ARG, "negative option");
+
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.sq = q_len; p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.window_left = window_left < 0 ? -1 : window_left;
+    p.flags = mask_flags(p.causal, p.window_left);
+    p.kv_len.assign(kv_len_host, kv_len_host + B);
+    p.kv_off.assign(size_t(B) + 1, 0);
+    long long total = 0;
+    for (int b = 0; b < B; ++b) {
+        if (p.kv_len[b] < 0 || p.kv_len[b] > kMaxSeqLen)
+            return fail(SK_ERR_INVALID_ARG, "kv_len entries must be in [0, 2^29]");
+        p.kv_off[size_t(b)] = total;
+        total += p.kv_len[b];
+        p.max_kv = std::max(p.max_kv, p.kv_len[b]);
+        if (p.kv_len[b] != p.kv_len[0]) p.varlen = true;
+    }
+    p.kv_off[size_t(B)] = total;
+    if (total >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "at most 2^31 - 1 KV rows in total");
+    if (p.varlen && B > kMaxVarlenBatch)
+        return fail(SK_ERR_UNSUPPORTED, "sequences of different lengths: at most 1024 per call");
+
+    p.num_sms = opts.num_sms > 0 ? opts.num_sms : device_num_sms;
+    if (p.num_sms <= 0) return fail(SK_ERR_INVALID_ARG, "unknown SM count");
+
+    // GQA packing (tiling chapter section 6.2), judged against the 128-row tile.
+    bool pack = should_pack_gqa(false, q_len, p.G, 128);
+    if (opts.force_pack_gqa == 1) pack = true;
+    if (opts.force_pack_gqa == -1) pack = false;
+    if (p.G == 1) pack = false;
+    p.pack_gqa = pack;
+    p.head_tiles = pack ? Hkv : Hq;
+    const long long rows = (long long)q_len * (pack ? p.G : 1);
+    if (rows > kMaxSeqLen) return fail(SK_ERR_UNSUPPORTED, "q_len * G too large");
+    p.rows = int(rows);
+
+    // Kernel choice: at most 64 packed rows -> decode kernel (KV rows on MMA M).
+    int path = opts.force_path;
+    if (path == SK_PATH_AUTO) path = (p.rows <= kDecodeMaxRows) ? SK_PATH_DECODE : SK_PATH_PREFILL;
+    if (path == SK_PATH_DECODE && p.rows > kDecodeMaxRows)
+        return fail(SK_ERR_UNSUPPORTED, "decode path holds at most 64 packed rows per tile");
+    p.path = path;
+    p.kBlockN = 128;
+    if (path == SK_PATH_DECODE) {
+        p.kBlockM = std::max(16, (p.rows + 15) / 16 * 16);
+    } else {
+        p.kBlockM = 128;
+    }
+    p.num_m_blocks = p.rows == 0 ? 0 : ceil_div_c(p.rows, p.kBlockM);
+    p.nblk_max = ceil_div_c(p.max_kv, p.kBlockN);
+    p.reverse_m = p.causal || p.window_left >= 0;
+
+    // Split count.
+    const int max_splits = std::max(
+        1, std::min(std::min(opts.max_splits > 0 ? opts.max_splits : kDefaultMaxSplits, kMaxSplits),
+                    std::max(p.nblk_max, 1)));
+    int S = 1;
+    const long long tiles = (long long)B * p.head_tiles * p.num_m_blocks;
+    if (opts.force_num_splits > 0) {
+        S = std::min(std::min(opts.force_num_splits, kMaxSplits), std::max(p.nblk_max, 1));
+    } else {
+        switch (opts.policy) {
+            case SK_POLICY_FA_HEURISTIC: {
+                const long long kv_head_bytes = (long long)p.max_kv * (2LL * d) * 2;
+                S = num_splits_fa_heuristic(int(std::min<long long>(tiles, 1LL << 30)), p.num_sms,
+                                            p.nblk_max, p.num_m_blocks, kv_head_bytes,
+                                            p.causal || p.window_left >= 0, max_splits);
+                break;
+            }
+            case SK_POLICY_FIXED_CHUNK:
+                S = std::max(1, std::min(32, ceil_div_c(p.max_kv, 2048)));
+                break;
+            case SK_POLICY_MIN_CHUNK: {
+                const int fill = int(std::min<long long>(
+                    (2LL * p.num_sms + std::max(tiles, 1LL) - 1) / std::max(tiles, 1LL), 1 << 20));
+                S = std::max(1, std::min(fill, p.max_kv / 256));
+                break;
+            }
+            default:
+                S = fill_policy(p, p.num_sms, max_splits);
+                break;
+        }
+        S = std::max(1, std::min(S, max_splits));
+    }
+    p.num_splits_policy = S;
+    p.splits_b = per_sequence_splits(p.kv_len, p.kBlockN, S);
+    p.num_splits = 1;
+    for (int c : p.splits_b) p.num_splits = std::max(p.num_splits, c);
+    p.needs_combine = p.num_splits > 1;
+
+    p.grid_x = p.num_m_blocks;
+    p.grid_y = p.head_tiles * p.num_splits;
+    p.grid_z = B;
+    if (p.grid_y > 65535) return fail(SK_ERR_UNSUPPORTED, "heads x splits exceeds 65535");
+    p.num_ctas = (long long)p.grid_x * p.grid_y * p.grid_z;
+
+    // Workspace: [status header 256 B][plan echo][LSE partials][O partials].
+    size_t off = 256;
+    p.echo_off = off;
+    off = align_up(off + size_t(p.num_ctas) * 16, 256);
+    p.lse_off = off;
+    if (p.needs_combine) {
+        const size_t rows_all = size_t(p.num_splits) * B * Hq * size_t(q_len);
+        off = align_up(off + rows_all * 4, 256);
+        p.o_off = off;
+        off = align_up(off + rows_all * size_t(d) * 4, 256);
+    } else {
+        p.o_off = off;
+    }
+    p.ws_bytes = off;
+    *out = std::move(p);
+    return SK_OK;
+}
+
+void plan_ranges(const Plan& p, int32_t* out) {
+    long long idx = 0;
+    for (int bz = 0; bz < p.grid_z; ++bz)
+        for (int by = 0; by < p.grid_y; ++by)
+            for (int bx = 0; bx < p.grid_x; ++bx, ++idx) {
+                const TileCoord t = tile_of_cta(bx, by, bz, p.num_m_blocks, p.num_splits, p.reverse_m);
+                const int sb = p.splits_b[size_t(t.batch)];
+                const uint32_t word = split_word(t.split, sb);
+                int32_t* e = out + idx * 4;
+                if (t.split >= sb) {
+                    e[0] = 0; e[1] = 0; e[2] = int32_t(word); e[3] = 0;
+                    continue;
+                }
+                const BlockRange r = n_block_range(p.sq, p.kv_len[size_t(t.batch)], t.m_block,
+                                                   p.kBlockM, p.kBlockN, p.flags, p.pack_gqa, p.G,
+                                                   word);
+                e[0] = r.lo; e[1] = r.hi; e[2] = int32_t(word); e[3] = 1;
+            }
+}
+
+void plan_to_info(const Plan& p, sk_attn_plan_info* info) {
+    memset(info, 0, sizeof *info);
+    info->path = p.path;
+    info->kBlockM = p.kBlockM;
+    info->kBlockN = p.kBlockN;
+    info->pack_gqa = p.pack_gqa ? 1 : 0;
+    info->head_tiles = p.head_tiles;
+    info->rows_per_head_tile = p.rows;
+    info->num_m_blocks = p.num_m_blocks;
+    info->num_splits = p.num_splits;
+    info->num_splits_policy = p.num_splits_policy;
+    info->num_n_blocks_max = p.nblk_max;
+    info->grid_x = p.grid_x;
+    info->grid_y = p.grid_y;
+    info->grid_z = p.grid_z;
+    info->num_ctas = p.num_ctas;
+    info->needs_combine = p.needs_combine ? 1 : 0;
+    info->workspace_bytes = p.ws_bytes;
+    info->echo_offset = p.echo_off;
+    info->lse_part_offset = p.lse_off;
+    info->o_part_offset = p.o_off;
+}
+
+}  // namespace sk

@@ -1,0 +1,61 @@
+// plan.h -- host scheduler for the split-KV attention forward (no CUDA needed).
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/sk_attn.h"
+#include "block_range.h"
+
+namespace sk {
+
+constexpr int kMaxVarlenBatch = 1024;   // per-sequence tables travel as kernel parameters
+constexpr int kDecodeMaxRows = 64;      // decode path: <= 64 packed rows per tile
+constexpr int kDefaultMaxSplits = 128;
+constexpr int kMaxSplits = 128;         // the combine kernel merges at most 128 partials
+
+struct Plan {
+    // problem
+    int B = 0, Hq = 0, Hkv = 0, G = 1, sq = 0, d = 0;
+    int causal = 0, window_left = -1;
+    MaskFlags flags{};
+    bool varlen = false;       // kv lengths differ between sequences
+    std::vector<int> kv_len;   // [B]
+    std::vector<long long> kv_off;  // [B + 1]
+    int max_kv = 0;
+    // decisions
+    int path = SK_PATH_AUTO;
+    int kBlockM = 0, kBlockN = 128;
+    bool pack_gqa = false;
+    int head_tiles = 0, rows = 0, num_m_blocks = 0;
+    int nblk_max = 0;
+    int num_splits_policy = 1, num_splits = 1;
+    std::vector<int> splits_b;  // [B] per-sequence split counts
+    bool needs_combine = false;
+    bool reverse_m = false;
+    int grid_x = 0, grid_y = 0, grid_z = 0;
+    long long num_ctas = 0;
+    int num_sms = 0;
+    // workspace
+    size_t ws_bytes = 0, echo_off = 0, lse_off = 0, o_off = 0;
+};
+
+// Builds the plan; on error returns the status and sets *why.
+sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int causal,
+                    int window_left, const sk_attn_opts* opts, int device_num_sms, Plan* plan,
+                    std::string* why);
+
+// Host-side range table (see sk_attn_plan_ranges).
+void plan_ranges(const Plan& p, int32_t* out);
+
+// The policies, exposed for tests through the plan.
+int num_splits_fa_heuristic(int total_mblocks, int num_sms, int num_n_blocks, int num_m_blocks,
+                            long long size_one_kv_head, bool is_causal_or_local, int max_splits);
+bool should_pack_gqa(bool varlen_q, int seqlen_q, int qhead_per_khead, int block_m);
+std::vector<int> per_sequence_splits(const std::vector<int>& kv_len, int block_n, int num_splits);
+
+void plan_to_info(const Plan& p, sk_attn_plan_info* info);
+
+}  // namespace sk

@@ -1,0 +1,109 @@
+"""CPU checks of the C ABI: the library builds and loads, exports every entry
+point that include/sk_attn.h declares, and rejects bad arguments in the host
+scheduler without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sk():
+    from split_kv_flash_gb300 import build as b
+    b.build()
+    import split_kv_flash_gb300 as sk
+    sk.lib()
+    return sk
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(sk_[a-z0-9_]+)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(sk):
+    names = _declared_symbols()
+    assert {"sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd", "sk_attn_read_plan_echo",
+            "sk_attn_workspace_status", "sk_attn_status_string", "sk_attn_last_error",
+            "sk_attn_version"} <= names
+    lib = ctypes.CDLL(sk.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), "symbol %s declared but not exported" % n
+
+
+def test_version_and_status_strings(sk):
+    assert sk.sk_attn_version() == 100
+    assert sk.sk_attn_status_string(0) == "SK_OK"
+    assert sk.sk_attn_status_string(6) == "SK_ERR_DEVICE_TIMEOUT"
+    assert sk.sk_attn_status_string(99) == "SK_ERR_UNKNOWN"
+
+
+def _opts(sk, **kw):
+    o = sk.Opts()
+    o.num_sms = kw.pop("num_sms", 148)
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(B=0), 1), (dict(Hq=6, Hkv=4), 1), (dict(d=96), 2), (dict(kv=[-1]), 1),
+    (dict(q_len=-1), 1), (dict(Hq=0), 1), (dict(kv=[1 << 30]), 1),
+])
+def test_plan_rejects_bad_arguments(sk, args, status):
+    a = dict(B=1, Hq=8, Hkv=2, q_len=1, kv=[100], d=128)
+    a.update(args)
+    kv = a["kv"] if len(a["kv"]) == max(a["B"], 1) else a["kv"] * max(a["B"], 1)
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_attn_plan(a["B"], a["Hq"], a["Hkv"], a["q_len"], kv, a["d"], opts=_opts(sk))
+    assert ei.value.status == status
+    assert sk.sk_attn_last_error() != ""
+
+
+def test_plan_rejects_bad_options(sk):
+    for kw in (dict(policy=9), dict(force_path=7), dict(force_pack_gqa=2), dict(max_splits=-3)):
+        with pytest.raises(sk.SKError) as ei:
+            sk.sk_attn_plan(1, 8, 2, 1, [100], 128, opts=_opts(sk, **kw))
+        assert ei.value.status == 1
+
+
+def test_decode_path_needs_small_tiles(sk):
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_attn_plan(1, 16, 16, 100, [500], 128, opts=_opts(sk, force_path=sk.SK_PATH_DECODE))
+    assert ei.value.status == 2
+
+
+def test_workspace_layout_is_aligned_and_sized(sk):
+    info = sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=_opts(sk, num_sms=152))
+    assert info.needs_combine == 1
+    S = info.num_splits
+    assert info.echo_offset == 256
+    for off in (info.lse_part_offset, info.o_part_offset, info.workspace_bytes):
+        assert off % 256 == 0
+    assert info.o_part_offset - info.lse_part_offset >= S * 32 * 4
+    assert info.workspace_bytes - info.o_part_offset >= S * 32 * 128 * 4
+    # no split -> no partial buffers
+    info1 = sk.sk_attn_plan(4, 32, 8, 8192, [8192] * 4, 128, causal=True, opts=_opts(sk))
+    assert info1.needs_combine == 0
+    assert info1.workspace_bytes == info1.o_part_offset
+
+
+def test_fwd_without_gpu_fails_cleanly(sk):
+    """No GPU here: the call must return an error status, never compute on the CPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_attn_fwd(16, 16, 16, 16, 16, 1, 4, 4, 1, [256], 64, 0.125, 0, -1, 256, 1 << 20)
+    assert ei.value.status in (2, 5)

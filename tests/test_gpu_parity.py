@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded bf16 inputs.  Tolerances: max-abs 8e-3 on O, 1e-3 on LSE."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sk():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    return H.sk_mod()
+
+
+def _check_full(sk, w, opts=None, tag=None):
+    q, k, v = wl.make_inputs(w)
+    out, lse = H.run_gpu(sk, w, q, k, v, opts)
+    ref_o, ref_l = H.oracle_full(w, q, k, v)
+    return H.compare_full(out, lse, ref_o, ref_l, tag or w.name)
+
+
+def _check_sampled(sk, w, n_rows, opts=None):
+    q, k, v = wl.make_inputs(w)
+    out, lse = H.run_gpu(sk, w, q, k, v, opts)
+    rows = H.sample_rows(w, n_rows)
+    ref_o, ref_l = oracle.attn_rows(wl.bits(q), wl.bits(k), wl.bits(v), w.kv_len, w.scale, rows,
+                                    w.causal, w.window_left)
+    return H.compare_rows(out, lse, rows, ref_o, ref_l, w.name)
+
+
+# ------------------------------------------------------------ the workloads
+
+def test_tiny_decode(sk):
+    _check_full(sk, wl.tiny_decode())
+
+
+@pytest.mark.parametrize("kv", [4096, 16384, 32768, 131072])
+def test_gqa_decode(sk, kv):
+    _check_full(sk, wl.gqa_decode(kv))
+
+
+@pytest.mark.parametrize("q_len", [9, 17, 33])
+@pytest.mark.parametrize("prefix", [128, 512, 2048, 8192])
+def test_spec_verify(sk, q_len, prefix):
+    _check_full(sk, wl.spec_verify(q_len, prefix))
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 8])
+def test_varlen_decode(sk, B):
+    _check_full(sk, wl.varlen_decode(B))
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_varlen_decode_large(sk, B):
+    _check_sampled(sk, wl.varlen_decode(B), 192)
+
+
+@pytest.mark.parametrize("local", [False, True])
+def test_prefill_8192(sk, local):
+    _check_sampled(sk, wl.prefill(local), 384)
+
+
+# ----------------------------------------------------------- shapes and edges
+
+EDGE = [
+    # name, B, Hq, Hkv, d, q_len, kv_len, causal, window
+    ("prefill_ragged_d128", 2, 4, 2, 128, 200, [333, 200], True, -1),
+    ("prefill_ragged_d64", 1, 2, 1, 64, 300, [300], True, -1),
+    ("prefill_packed_gqa", 1, 16, 2, 128, 33, [1000], True, -1),
+    ("prefill_local", 1, 4, 4, 128, 520, [520], True, 100),
+    ("prefill_window_no_causal", 1, 2, 2, 128, 150, [400], False, 60),
+    ("prefill_sk_lt_sq", 1, 2, 2, 128, 260, [100], True, -1),
+    ("decode_d64_gqa", 3, 8, 2, 64, 1, [1, 129, 1000], False, -1),
+    ("decode_empty_seq", 3, 4, 4, 128, 1, [0, 5, 256], False, -1),
+    ("decode_window", 2, 8, 8, 128, 3, [700, 90], False, 33),
+    ("decode_causal_window", 1, 8, 2, 128, 8, [1000], True, 0),
+    ("decode_unpacked_gqa", 1, 8, 4, 128, 30, [500], True, -1),
+    ("verify_sk_lt_sq", 1, 4, 4, 128, 40, [20], True, -1),
+    ("decode_kv_not_multiple", 1, 4, 1, 128, 1, [127], False, -1),
+    ("decode_rows_64", 1, 64, 1, 128, 1, [3000], False, -1),
+    ("decode_rows_48", 1, 16, 1, 128, 3, [3000], False, -1),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[c[0] for c in EDGE])
+def test_edge_shapes(sk, case):
+    name, B, Hq, Hkv, d, sq, kv, causal, window = case
+    w = wl.Workload(name, B, Hq, Hkv, d, sq, kv, causal=causal, window_left=window, seed=77)
+    opts = None
+    if name == "decode_unpacked_gqa":
+        opts = sk.Opts()
+        opts.force_pack_gqa = -1
+    _check_full(sk, w, opts)
+
+
+def test_q_len_zero_is_a_no_op(sk):
+    q = torch.empty((1, 0, 4, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.randn((64, 4, 128), device="cuda").to(torch.bfloat16)
+    out, lse, _ = sk.attn_fwd(q, k, k.clone(), [64])
+    assert out.numel() == 0 and lse.numel() == 0
+
+
+# ------------------------------------------------------- split invariance
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 32, 128])
+def test_forced_splits(sk, S):
+    w = wl.gqa_decode(16384)
+    opts = sk.Opts()
+    opts.force_num_splits = S
+    _check_full(sk, w, opts, "%s_S%d" % (w.name, S))
+
+
+@pytest.mark.parametrize("policy", [1, 2, 3, 4])
+def test_policies(sk, policy):
+    w = wl.gqa_decode(32768)
+    opts = sk.Opts()
+    opts.policy = policy
+    _check_full(sk, w, opts, "%s_policy%d" % (w.name, policy))
+
+
+def test_prefill_path_with_splits(sk):
+    w = wl.Workload("prefill_split", 1, 4, 2, 128, 256, [2048], causal=True, seed=5)
+    opts = sk.Opts()
+    opts.force_num_splits = 5
+    _check_full(sk, w, opts)
+
+
+def test_decode_forced_onto_prefill_kernel(sk):
+    w = wl.gqa_decode(4096)
+    opts = sk.Opts()
+    opts.force_path = sk.SK_PATH_PREFILL
+    _check_full(sk, w, opts, "gqa_decode_on_prefill_kernel")

@@ -1,0 +1,136 @@
+"""The product's host scheduler (libskattn.so, sk_attn_plan / sk_attn_plan_ranges)
+against the scheduling oracle written from the pages: packing decision, split
+counts of the page-derived policies, per-sequence split counts and the KV block
+range of every CTA must match bit for bit.  The GPU echo test then checks that
+the kernels use exactly these ranges."""
+import numpy as np
+import pytest
+
+from oracle import plan_oracle as po
+import workloads as wl
+
+
+@pytest.fixture(scope="module")
+def sk():
+    from split_kv_flash_gb300 import build as b
+    b.build()
+    import split_kv_flash_gb300 as sk
+    return sk
+
+
+POLICIES = {"fa": 2, "fixed_chunk": 3, "min_chunk": 4}
+
+
+def _opts(sk, policy=0, num_sms=148, **kw):
+    o = sk.Opts()
+    o.policy = policy
+    o.num_sms = num_sms
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def _expected(sk, info, B, Hq, Hkv, sq, kv, d, causal, window, policy, num_sms, force_splits=0):
+    G = Hq // Hkv
+    pack = po.should_pack_gqa(False, sq, G, 128) and G > 1
+    assert bool(info.pack_gqa) == pack
+    head_tiles = Hkv if pack else Hq
+    assert info.head_tiles == head_tiles
+    rows = sq * (G if pack else 1)
+    assert info.rows_per_head_tile == rows
+    nm = po.ceil_div(rows, info.kBlockM) if rows else 0
+    assert info.num_m_blocks == nm
+    if force_splits:
+        S = min(force_splits, 128, max(po.ceil_div(max(kv), 128), 1))
+    else:
+        S = po.choose_splits(policy, B, head_tiles, nm, kv, d, 128, num_sms, causal or window >= 0)
+    assert info.num_splits_policy == S
+    sb = po.split_counts(kv, 128, S)
+    assert info.num_splits == max(sb)
+    return po.cta_table(sq, kv, G, pack, head_tiles, info.kBlockM, 128, nm, info.num_splits, sb,
+                        causal, window)
+
+
+def _cases():
+    rng = np.random.default_rng(1234)
+    cases = [
+        # the workloads' shapes
+        (1, 4, 4, 1, [256], 64, False, -1),
+        (1, 32, 4, 1, [4096], 128, False, -1),
+        (1, 32, 4, 1, [131072], 128, False, -1),
+        (2, 16, 16, 9, [128 + 9] * 2, 128, True, -1),
+        (2, 16, 16, 33, [8192 + 33] * 2, 128, True, -1),
+        (4, 32, 8, 1, wl.varlen_lengths(4, 1302), 128, False, -1),
+        (32, 32, 8, 1, wl.varlen_lengths(32, 1305), 128, False, -1),
+        (4, 32, 8, 8192, [8192] * 4, 128, True, -1),
+        (4, 32, 8, 8192, [8192] * 4, 128, True, 1024),
+        # edge cases: ragged, empty sequences, window without causal, sk < sq
+        (3, 8, 2, 5, [0, 1, 300], 64, True, -1),
+        (2, 12, 3, 40, [17, 1000], 128, False, 50),
+        (1, 2, 1, 200, [150], 128, True, 7),
+        (1, 64, 8, 2, [999], 64, True, 0),
+    ]
+    for _ in range(60):
+        B = int(rng.integers(1, 9))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        sq = int(rng.choice([1, 2, 5, 9, 17, 33, 64, 100, 300]))
+        if rng.random() < 0.5:
+            kv = [int(rng.integers(0, 5000))] * B
+        else:
+            kv = [int(x) for x in rng.integers(0, 9000, size=B)]
+        causal = bool(rng.integers(0, 2))
+        window = int(rng.choice([-1, -1, 0, 33, 1024]))
+        cases.append((B, Hkv * G, Hkv, sq, kv, int(rng.choice([64, 128])), causal, window))
+    return cases
+
+
+@pytest.mark.parametrize("policy", sorted(POLICIES))
+def test_plan_matches_oracle(sk, policy):
+    for num_sms in (108, 148, 152):
+        for (B, Hq, Hkv, sq, kv, d, causal, window) in _cases():
+            o = _opts(sk, POLICIES[policy], num_sms)
+            info = sk.sk_attn_plan(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            exp = _expected(sk, info, B, Hq, Hkv, sq, kv, d, causal, window, policy, num_sms)
+            got = sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            assert got == exp, (B, Hq, Hkv, sq, kv, d, causal, window, policy, num_sms)
+
+
+def test_forced_split_counts_match_oracle(sk):
+    for S in (1, 2, 3, 7, 40, 128, 500):
+        for (B, Hq, Hkv, sq, kv, d, causal, window) in _cases()[:20]:
+            o = _opts(sk, 0, 148, force_num_splits=S)
+            info = sk.sk_attn_plan(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            exp = _expected(sk, info, B, Hq, Hkv, sq, kv, d, causal, window, None, 148, S)
+            got = sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            assert got == exp
+
+
+def test_fill_policy_invariants(sk):
+    """The default policy (own, measured choice): splits tile each range exactly,
+    every CTA fits in one wave when splitting, and no split repeats a chunk."""
+    for num_sms in (148, 152):
+        for (B, Hq, Hkv, sq, kv, d, causal, window) in _cases():
+            o = _opts(sk, 0, num_sms)
+            info = sk.sk_attn_plan(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            S = info.num_splits_policy
+            sb = po.split_counts(kv, 128, S)
+            assert info.num_splits == max(sb)
+            if info.needs_combine:
+                ctas = sum(c * info.head_tiles * info.num_m_blocks for c in sb)
+                assert ctas <= num_sms
+            G = Hq // Hkv
+            pack = bool(info.pack_gqa)
+            exp = po.cta_table(sq, kv, G, pack, info.head_tiles, info.kBlockM, 128,
+                               info.num_m_blocks, info.num_splits, sb, causal, window)
+            assert sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, o) == exp
+
+
+def test_gqa_decode_split_counts(sk):
+    """GQA decode at 131072 keys: the section 5.2 heuristic gives 32 splits on
+    148 SMs (4 tiles); the default policy fills all 152 SMs of a GB300."""
+    info = sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=_opts(sk, POLICIES["fa"], 148))
+    assert info.num_splits_policy == 32
+    info = sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=_opts(sk, 0, 152))
+    assert info.num_splits == 38 and info.num_ctas == 152
+    assert info.path == sk.SK_PATH_DECODE and info.kBlockM == 16 and info.pack_gqa == 1

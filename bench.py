@@ -1,0 +1,497 @@
+"""Benchmark of the split-KV flash attention forward on GB300.
+
+Headline (one JSON line on rank 0): small-grid long-context GQA decode,
+B=1, Hq=32, Hkv=4, d=128, q_len=1, kv_len=131072 (Qwen3-30B-A3B-like, K scaled
+by 0.5), as achieved HBM GB/s of algorithmic bytes (K + V + Q read, O + LSE
+written).  One step = one sk_attn_fwd call through the C ABI: host plan,
+partial (split) kernel, combine kernel.  The long causal prefill
+(B=4, Hq=32, Hkv=8, d=128, 8192 x 8192) is reported beside it as TFLOP/s of
+visible (query, key) pairs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (one process per GPU under torch.distributed.run) every rank runs
+its own independent decode problem (no collective on the data path); value is
+the bytes of all ranks divided by the slowest rank's time (weak scaling).
+--impl reference times the fp64 CPU oracle on the host cores instead (rank 0
+only), on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "decode attn HBM GB/s (% of peak) and prefill TFLOP/s (% of peak), 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--kv", type=int, default=131072)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------- env
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, bf16, bf16_sus, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+
+            def find(keys):
+                for k in keys:
+                    if k in d and isinstance(d[k], (int, float)):
+                        return float(d[k])
+                return None
+            h = find(["hbm_gbs", "hbm_GBps", "hbm_copy_gbs"])
+            b = find(["bf16_tflops", "bf16_dense_tflops"])
+            bs = find(["bf16_tflops_sustained"])
+            if h:
+                hbm, src = h, "measured"
+            if b:
+                bf16 = b
+            if bs:
+                bf16_sus = bs
+        except Exception:  # noqa: BLE001
+            pass
+    return hbm, bf16, bf16_sus, src
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def file_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+DECODE_SOURCES = ["split_kv_flash_gb300/csrc/fwd_decode.cu", "split_kv_flash_gb300/csrc/sm103_ptx.cuh",
+                  "split_kv_flash_gb300/csrc/fwd_common.cuh", "split_kv_flash_gb300/csrc/block_range.h"]
+PREFILL_SOURCES = ["split_kv_flash_gb300/csrc/fwd_prefill.cu", "split_kv_flash_gb300/csrc/sm103_ptx.cuh",
+                   "split_kv_flash_gb300/csrc/fwd_common.cuh", "split_kv_flash_gb300/csrc/block_range.h"]
+
+
+def ncu_traffic(kernel_key, sources):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path)).get(kernel_key)
+        if d and d.get("source_sha") == file_sha(sources):
+            return float(d["dram_bytes_per_launch"])
+    except Exception:  # noqa: BLE001
+        pass
+    return None
+
+
+# --------------------------------------------------------------- workloads
+def decode_bytes(w):
+    kv = 2 * w.total_kv * w.Hkv * w.d * 2
+    q = w.B * w.q_len * w.Hq * w.d * 2
+    o = q
+    lse = w.B * w.Hq * w.q_len * 4
+    return kv + q + o + lse
+
+
+def visible_pairs(w):
+    n = 0
+    for sk_b in w.kv_len:
+        sq = w.q_len
+        for i in range(sq):
+            diag = i + sk_b - sq
+            hi = min(sk_b - 1, diag) if w.causal else sk_b - 1
+            lo = max(0, diag - w.window_left) if w.window_left >= 0 else 0
+            n += max(0, hi - lo + 1)
+    return n * w.Hq
+
+
+def prefill_flops(w):
+    # QK^T and PV: 2 * d flops each per visible (query, key, head)
+    return 4.0 * w.d * visible_pairs(w)
+
+
+# --------------------------------------------------------------- GPU arm
+def gpu_decode(sk, w, steps, warmup, device, rotate=3):
+    q, k, v = wl.make_inputs(w)
+    qs = [q.to(device) for _ in range(rotate)]
+    kv_dev = k.to(device), v.to(device)
+    ks = [kv_dev[0]] + [kv_dev[0].clone() for _ in range(rotate - 1)]
+    vs = [kv_dev[1]] + [kv_dev[1].clone() for _ in range(rotate - 1)]
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left)
+    outs = [torch.empty((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+            for _ in range(rotate)]
+    lses = [torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
+            for _ in range(rotate)]
+    ws = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    ptrs = [(qs[i].data_ptr(), ks[i].data_ptr(), vs[i].data_ptr(), outs[i].data_ptr(),
+             lses[i].data_ptr()) for i in range(rotate)]
+    opts = sk.Opts()
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in ev_b + ev_e:
+        e.record(stream)
+    L = sk.lib()
+    arr, _ = sk._kv_array(w.kv_len)
+    ws_ptr, ws_n = ws.data_ptr(), ws.numel()
+
+    def call(i, with_events=None):
+        p = ptrs[i % rotate]
+        if with_events is not None:
+            opts.event_begin = ev_b[with_events].cuda_event
+            opts.event_end = ev_e[with_events].cuda_event
+        else:
+            opts.event_begin = None
+            opts.event_end = None
+        st = L.sk_attn_fwd(p[0], p[1], p[2], p[3], p[4], w.B, w.Hq, w.Hkv, w.q_len, arr, w.d,
+                           w.scale, int(w.causal), w.window_left, ws_ptr, ws_n, sh,
+                           __import__("ctypes").byref(opts))
+        if st != 0:
+            raise RuntimeError("sk_attn_fwd: " + sk.sk_attn_last_error())
+
+    for i in range(warmup):
+        call(i)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(device)
+    t0.record(stream)
+    for i in range(steps):
+        call(i, with_events=i)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(steps)]
+    st, where = sk.sk_attn_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d at %d" % (st, where))
+    return total_ms, kern_ms, info
+
+
+def gpu_e2e(sk, w, steps, device):
+    """Host buffers in, host buffers out: H2D of Q, K, V from pinned memory,
+    sk_attn_fwd, D2H of O and LSE, every step, inside the timed region."""
+    q, k, v = wl.make_inputs(w)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    qd, kd, vd = (torch.empty_like(t, device=device) for t in (q, k, v))
+    out_h = torch.empty((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32).pin_memory()
+    out_d = torch.empty(out_h.shape, dtype=torch.bfloat16, device=device)
+    lse_d = torch.empty(lse_h.shape, dtype=torch.float32, device=device)
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left)
+    ws = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        sk.sk_attn_fwd(qd, kd, vd, out_d, lse_d, w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.scale,
+                       w.causal, w.window_left, ws, ws.numel(), stream)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return ms, h2d, d2h
+
+
+def gpu_prefill(sk, w, steps, warmup, device):
+    q, k, v = wl.make_inputs(w)
+    qd, kd, vd = q.to(device), k.to(device), v.to(device)
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left)
+    out = torch.empty((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
+    ws = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    opts = sk.Opts()
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    eve = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in evb + eve:
+        e.record(stream)
+    for _ in range(warmup):
+        sk.sk_attn_fwd(qd, kd, vd, out, lse, w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.scale,
+                       w.causal, w.window_left, ws, ws.numel(), stream, opts)
+    torch.cuda.synchronize(device)
+    for i in range(steps):
+        flush.fill_(float(i))  # L2 flush between timed launches (outside the events)
+        opts.event_begin = evb[i].cuda_event
+        opts.event_end = eve[i].cuda_event
+        sk.sk_attn_fwd(qd, kd, vd, out, lse, w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.scale,
+                       w.causal, w.window_left, ws, ws.numel(), stream, opts)
+    torch.cuda.synchronize(device)
+    ms = [evb[i].elapsed_time(eve[i]) for i in range(steps)]
+    return statistics.median(ms), info
+
+
+_pg = None
+
+
+def barrier():
+    if _pg is not None:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x):
+    if _pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU arm
+def cpu_oracle(w, seconds, rows_per_call=None):
+    """Time the fp64 oracle on the host cores on whole query rows of w: each
+    call computes `rows_per_call` (b, h, i) rows; value in GB/s of the
+    algorithmic bytes those rows stand for."""
+    import oracle
+    q, k, v = wl.make_inputs(w)
+    qb, kb, vb = wl.bits(q), wl.bits(k), wl.bits(v)
+    all_rows = np.array([(b, h, i) for b in range(w.B) for h in range(w.Hq) for i in range(w.q_len)],
+                        dtype=np.int32)
+    n = rows_per_call or len(all_rows)
+    rows = all_rows[:n]
+    threads = os.cpu_count() or 1
+    oracle.attn_rows(qb, kb, vb, w.kv_len, w.scale, rows[:1], w.causal, w.window_left, threads)
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        oracle.attn_rows(qb, kb, vb, w.kv_len, w.scale, rows, w.causal, w.window_left, threads)
+        calls += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / calls
+    frac = n / len(all_rows)
+    gbs = decode_bytes(w) * frac / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d query rows of %s per call, %d calls, %.1f s" % (
+                n, len(all_rows), w.name, calls, dt * calls),
+            "seconds_per_call": dt}
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    w = wl.gqa_decode(args.kv)
+    steps, warmup = args.steps, args.warmup
+    # each step: the oracle on every query row of the decode step (32 rows x
+    # 131072 keys); at most 20 steps keep the run within minutes.
+    budget_steps = max(1, min(steps, 20))
+    import oracle
+    q, k, v = wl.make_inputs(w)
+    qb, kb, vb = wl.bits(q), wl.bits(k), wl.bits(v)
+    rows = np.array([(b, h, i) for b in range(w.B) for h in range(w.Hq) for i in range(w.q_len)],
+                    dtype=np.int32)
+    threads = os.cpu_count() or 1
+    for _ in range(min(warmup, 3)):
+        oracle.attn_rows(qb, kb, vb, w.kv_len, w.scale, rows, w.causal, w.window_left, threads)
+    t0 = time.perf_counter()
+    for _ in range(budget_steps):
+        oracle.attn_rows(qb, kb, vb, w.kv_len, w.scale, rows, w.causal, w.window_left, threads)
+    dt = (time.perf_counter() - t0) / budget_steps
+    frac = len(rows) / (w.B * w.Hq * w.q_len)
+    value = decode_bytes(w) * frac / dt / 1e9
+    sample = "all %d query rows of %s per step, %d steps" % (len(rows), w.name, budget_steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": budget_steps, "warmup": min(warmup, 3), "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "q_len": w.q_len, "kv_len": w.kv_len[0], "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main
+def main():
+    global _pg
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+        _pg = torch.distributed.group.WORLD
+    import split_kv_flash_gb300 as sk
+    from split_kv_flash_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    barrier()
+    sk.lib()
+
+    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+    w = wl.gqa_decode(args.kv)
+    with ClockSampler(local) as clk:
+        total_ms, kern_ms, info = gpu_decode(sk, w, args.steps, args.warmup, device)
+    total_ms = max_over_ranks(total_ms)
+    bytes_step = decode_bytes(w)
+    value = bytes_step * args.steps * world / (total_ms * 1e-3) / 1e9
+    kern_avg = float(np.mean(kern_ms))
+    achieved = bytes_step / (kern_avg * 1e-3) / 1e9
+    clocks = clk.summary()
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "q_len": w.q_len, "kv_len": w.kv_len[0], "k_scale": 0.5,
+                   "num_splits": info.num_splits, "ctas": info.num_ctas,
+                   "l2": "inputs larger than L2: 3 rotating copies of Q/K/V (%.0f MB each)" % (
+                       bytes_step / 1e6),
+                   "parallelism": "independent problem per GPU" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak,
+                     "traffic": ncu_traffic("decode_gqa_kv131072", DECODE_SOURCES),
+                     "kernel": "fwd_decode_kernel<128,16,UniformSeqs>",
+                     "kernel_ms": kern_avg, "peak_source": peak_src + " hbm_gbs"},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+    }
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 30))
+        ms, h2d, d2h = gpu_e2e(sk, w, e2e_steps, device)
+        ms = max_over_ranks(ms)
+        result["e2e"] = {"value": bytes_step * world / (ms * 1e-3) / 1e9, "unit": "GB/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "ms_per_step": ms, "steps": e2e_steps}
+    if not args.no_prefill:
+        pre = {}
+        for local_w in (False, True):
+            pw = wl.prefill(local_w)
+            ms, pinfo = gpu_prefill(sk, pw, 10, 3, device)
+            fl = prefill_flops(pw)
+            tf = fl / (ms * 1e-3) / 1e12
+            key = "local1024" if local_w else "causal"
+            pre[key] = {"workload": pw.name, "tflops": tf, "ms": ms, "flops": fl,
+                        "frac_of_bf16_peak": tf / bf16_peak}
+        result["prefill"] = {
+            "unit": "TFLOP/s", "peak": bf16_peak, "peak_source": peak_src + " bf16_tflops (burst)",
+            "flop_count": "4 * d per visible (query, key) pair per head", **pre,
+            "traffic": ncu_traffic("prefill_causal_8192", PREFILL_SOURCES)}
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if _pg is not None:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -294,16 +294,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar_odone, (j - 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
-            // The whole 128 rows must agree on whether O changes before the MMA;
-            // each row rescales its own lane, so no cross-thread step is needed.
-            if (rescale && j >= 1) {
+            // Each row rescales its own TMEM lane.  tcgen05.ld/st are warp-collective
+            // (.sync.aligned), so the whole warp enters together; rows that keep
+            // their max multiply by 1.
+            if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                const float a = rescale ? alpha : 1.f;
 #pragma unroll
                 for (int c = 0; c < HD / 16; ++c) {
                     float o[16];
                     tmem_ld16(tO + lane_off + c * 16, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] *= alpha;
+                    for (int e = 0; e < 16; ++e) o[e] *= a;
                     tmem_st16(tO + lane_off + c * 16, o);
                 }
                 tmem_wait_st();

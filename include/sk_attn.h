@@ -148,6 +148,35 @@ sk_status sk_attn_read_plan_echo(const void* workspace, int32_t* ranges_host, si
  * of the wait that expired. */
 sk_status sk_attn_workspace_status(void* workspace, void* cuda_stream, int* where);
 
+/* Attention forward for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for this
+ * library's users.  Code that must not call cudaMalloc / cudaFree (they can
+ * synchronise the device, so hot decode loops avoid them; some callers only
+ * own memory handed out by another runtime's pool) has no way to obtain the
+ * workspace that sk_attn_fwd wants.  This variant takes no workspace: the split
+ * kernels use one scratch array compiled into the library, of
+ * SK_NOALLOC_SCRATCH_BYTES bytes on every GPU that loads the library (held until
+ * the process exits).  It allocates no device memory and calls no allocating
+ * routine.
+ *   - Arguments, layouts, results and errors are those of sk_attn_fwd.
+ *   - A problem whose plan needs more than SK_NOALLOC_SCRATCH_BYTES of workspace
+ *     (sk_attn_plan_info.workspace_bytes) is rejected with
+ *     SK_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on each device looks up the scratch array's device address
+ *     (with that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the previous call's contents;
+ *     the call clears the status header it needs at zero (an asynchronous memset
+ *     on cuda_stream) before the kernels.  Calls whose work overlaps on the GPU
+ *     (different streams, or several host threads without ordering) race on the
+ *     scratch and give wrong results: order them on one stream.
+ *   - Device-side wait timeouts are not reported through this entry point. */
+#define SK_NOALLOC_SCRATCH_BYTES (16u << 20)
+sk_status sk_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
+                              float scale, int causal, int window_left, void* cuda_stream,
+                              const sk_attn_opts* opts);
+
 const char* sk_attn_status_string(sk_status s);
 /* One-line reason for the last error returned on this thread ("" if none). */
 const char* sk_attn_last_error(void);

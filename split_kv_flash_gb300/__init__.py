@@ -14,6 +14,7 @@ import os
 __all__ = [
     "SKError", "Opts", "PlanInfo", "lib", "sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd",
     "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_status_string",
+    "sk_attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
     "SK_PATH_PREFILL", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
@@ -27,6 +28,7 @@ SK_ERR_MISALIGNED, SK_ERR_CUDA, SK_ERR_DEVICE_TIMEOUT = 4, 5, 6
 SK_POLICY_DEFAULT, SK_POLICY_FILL, SK_POLICY_FA_HEURISTIC = 0, 1, 2
 SK_POLICY_FIXED_CHUNK, SK_POLICY_MIN_CHUNK = 3, 4
 SK_PATH_AUTO, SK_PATH_DECODE, SK_PATH_PREFILL = 0, 1, 2
+NOALLOC_SCRATCH_BYTES = 16 << 20  # SK_NOALLOC_SCRATCH_BYTES in include/sk_attn.h
 
 
 class Opts(ctypes.Structure):
@@ -84,10 +86,12 @@ def lib():
                                           _i32p, sz]
         L.sk_attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, _intp, ci, cf, ci, ci, vp, sz,
                                   vp, ctypes.POINTER(Opts)]
+        L.sk_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, _intp, ci, cf, ci, ci,
+                                          vp, ctypes.POINTER(Opts)]
         L.sk_attn_read_plan_echo.argtypes = [vp, _i32p, sz, vp]
         L.sk_attn_workspace_status.argtypes = [vp, vp, _intp]
-        for f in ("sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd", "sk_attn_read_plan_echo",
-                  "sk_attn_workspace_status"):
+        for f in ("sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd", "sk_attn_fwd_noalloc",
+                  "sk_attn_read_plan_echo", "sk_attn_workspace_status"):
             getattr(L, f).restype = ci
         L.sk_attn_status_string.argtypes = [ci]
         L.sk_attn_status_string.restype = ctypes.c_char_p
@@ -159,6 +163,21 @@ def sk_attn_fwd(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len, d, scale, causal, 
                              arr, d, float(scale), int(causal), int(window_left), _ptr(workspace),
                              int(ws_bytes), stream,
                              ctypes.byref(opts) if opts is not None else None))
+
+
+def sk_attn_fwd_noalloc(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len, d, scale, causal,
+                        window_left, stream=None, opts=None):
+    """Like sk_attn_fwd, but with no workspace argument: for callers that cannot
+    allocate device memory around the call.  The library's built-in scratch
+    (NOALLOC_SCRATCH_BYTES per GPU) is used instead; larger problems raise
+    SKError(SK_ERR_WORKSPACE_TOO_SMALL).  Calls that overlap on the GPU share
+    that scratch and race: keep them ordered on one stream."""
+    arr, _ = _kv_array(kv_len)
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _check(lib().sk_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                     q_len, arr, d, float(scale), int(causal), int(window_left),
+                                     stream, ctypes.byref(opts) if opts is not None else None))
 
 
 def sk_attn_read_plan_echo(workspace, num_ctas, stream=None):

@@ -91,6 +91,8 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
 cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
     static std::mutex mu;
     static std::set<std::pair<const void*, int>> done;

@@ -39,6 +39,10 @@ METRIC = "decode attn HBM GB/s (% of peak) and prefill TFLOP/s (% of peak), 1 GB
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
+# The partial kernel is bracketed by CUDA events on every 16th timed step only:
+# an event between the partial and the combine kernel keeps the combine from
+# being launched early (programmatic dependent launch), so most steps run without.
+EVENT_EVERY = 16
 
 
 def parse():
@@ -49,6 +53,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kv", type=int, default=131072)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="prefill only (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -229,6 +234,8 @@ def gpu_decode(sk, w, steps, warmup, device, rotate=3):
 
     def call(i, with_events=None):
         p = ptrs[i % rotate]
+        if with_events is not None and with_events % EVENT_EVERY != 0:
+            with_events = None
         if with_events is not None:
             opts.event_begin = ev_b[with_events].cuda_event
             opts.event_end = ev_e[with_events].cuda_event
@@ -255,7 +262,7 @@ def gpu_decode(sk, w, steps, warmup, device, rotate=3):
     torch.cuda.synchronize(device)
     barrier()
     total_ms = t0.elapsed_time(t1)
-    kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(steps)]
+    kern_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(0, steps, EVENT_EVERY)]
     st, where = sk.sk_attn_workspace_status(ws)
     if st != 0:
         raise RuntimeError("device status %d at %d" % (st, where))
@@ -436,6 +443,15 @@ def main():
     sk.lib()
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+    if args.no_decode:  # profiling helper: the prefill kernels alone
+        pre = {}
+        for local_w in (False, True):
+            pw = wl.prefill(local_w)
+            ms, _ = gpu_prefill(sk, pw, max(1, min(args.steps, 10)), max(1, args.warmup), device)
+            pre["local1024" if local_w else "causal"] = prefill_flops(pw) / (ms * 1e-3) / 1e12
+        if rank == 0:
+            print(json.dumps({"prefill_tflops": pre}), flush=True)
+        return
     w = wl.gqa_decode(args.kv)
     with ClockSampler(local) as clk:
         total_ms, kern_ms, info = gpu_decode(sk, w, args.steps, args.warmup, device)

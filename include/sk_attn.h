@@ -128,9 +128,10 @@ sk_status sk_attn_plan_ranges(int B, int Hq, int Hkv, int q_len, const int* kv_l
 
 /* Attention forward.  Asynchronous on cuda_stream (a cudaStream_t; NULL = legacy
  * default stream).  workspace: device buffer of >= info.workspace_bytes bytes,
- * 256-byte aligned, zero-filled once before its first use (the library keeps
- * its header valid afterwards); it may be reused by consecutive calls on the same
- * stream.  Returns SK_OK once the kernels are enqueued. */
+ * 256-byte aligned, zero-filled once before its first use (every call leaves its
+ * status word at zero unless a kernel timed out); it may be reused by consecutive
+ * calls on the same stream, but calls that overlap on the GPU need separate
+ * workspaces.  Returns SK_OK once the kernels are enqueued. */
 sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                       int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
                       float scale, int causal, int window_left,

@@ -199,6 +199,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     fp.o_part = reinterpret_cast<float*>(ws + p.o_off);
     fp.lse_part = reinterpret_cast<float*>(ws + p.lse_off);
     fp.echo = reinterpret_cast<int32_t*>(ws + p.echo_off);
+
     fp.status = reinterpret_cast<uint32_t*>(ws);
     fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.G = p.G; fp.sq = q_len; fp.d = d;
     fp.pack_gqa = p.pack_gqa ? 1 : 0;

@@ -23,6 +23,7 @@ enum : uint32_t {
     kSiteSoftmaxSFull = 6,
     kSiteSoftmaxODone = 7,
     kSiteInjected = 8,
+    kSiteSmemAlign = 9,
 };
 
 struct FwdParams {
@@ -90,6 +91,27 @@ cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorM
 cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 
 void fill_varlen(const Plan& plan, VarlenSeqs* v);
+
+// Launch a partial kernel as a programmatic dependent of the previous work on
+// the stream: it may be scheduled while that work drains and waits for it
+// (griddepcontrol.wait) before touching global memory.
+template <class Seqs>
+cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                       const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const Seqs& seqs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[4] = {const_cast<FwdParams*>(&p), const_cast<CUtensorMap*>(&tmK), const_cast<CUtensorMap*>(&tmV),
+                     const_cast<Seqs*>(&seqs)};
+    return cudaLaunchKernelExC(&cfg, kernel, args);
+}
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);

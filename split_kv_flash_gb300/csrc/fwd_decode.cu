@@ -20,6 +20,7 @@
 #include <math.h>
 
 #include "fwd_common.cuh"
+#include "kv_producer.cuh"
 #include "sm103_ptx.cuh"
 
 namespace sk {
@@ -48,14 +49,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <int HD, int NP>
 struct DecodeCfg {
-    static constexpr int kStages = HD == 128 ? (NP <= 32 ? 3 : 2) : 4;
+    static constexpr int kStages = HD == 128 ? (NP <= 32 ? 3 : 2) : (NP <= 32 ? 4 : 3);
     static constexpr int kKBytes = 128 * HD * 2;      // K block: 128 rows x HD
     static constexpr int kVBytes = 128 * 128 * 2;     // V block region: 128 rows x 128 (M = 128 for PV)
     static constexpr int kVLoadBytes = 128 * HD * 2;  // bytes actually loaded
-    static constexpr int kStageBytes = kKBytes + kVBytes;
+    static constexpr int kStageBytes = kKBytes + kVBytes;  // one K slot + one V slot
     static constexpr int kQBytes = NP * HD * 2;
-    static constexpr int kPBytes = NP * 128 * 2;
-    static constexpr int kOffStages = 0;
+    static constexpr int kPBuf = NP * 128 * 2;             // one P^T buffer
+    static constexpr int kPBytes = 2 * kPBuf;                // double-buffered
+    static constexpr int kOffK = 0;                        // K ring: kStages slots
+    static constexpr int kOffV = kStages * kKBytes;        // V ring: kStages slots
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffP = kOffQ + kQBytes;
     static constexpr int kOffRed = kOffP + kPBytes;            // float red[4][NP]
@@ -64,13 +67,14 @@ struct DecodeCfg {
     static constexpr int kOffL = kOffAlpha + NP * 4;           // float l[NP]
     static constexpr int kOffDiag = kOffL + NP * 4;            // int diag[NP]
     static constexpr int kOffBars = (kOffDiag + NP * 4 + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1 + 1 + 1;
+    static constexpr int kNumBars = 4 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;   // tmem base, abort flag
     static constexpr int kSmemBytes = kOffMisc + 16;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1024
     static constexpr int kTmemCols = (3 * NP <= 32) ? 32 : (3 * NP <= 64) ? 64 : (3 * NP <= 128) ? 128 : 256;
     static_assert(kSmemAlloc <= 232448, "shared memory budget");
-    static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "UMMA operands need 1024-byte alignment");
+    static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBuf % 1024 == 0 && kOffV % 1024 == 0,
+                  "UMMA operands need 1024-byte alignment");
 };
 
 template <int HD, int NP, class Seqs>
@@ -95,6 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long cta_lin =
         blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
     if (tc.split >= sb) {
+        griddep_launch_dependents();
+        griddep_wait();
         if (p.echo_plan && threadIdx.x == 0) {
             int4 e = make_int4(0, 0, int(word), 0);
             *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = e;
@@ -106,10 +112,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BlockRange br =
         n_block_range(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.flags, p.pack_gqa != 0, p.G, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
-    if (p.echo_plan && threadIdx.x == 0) {
-        int4 e = make_int4(br.lo, br.hi, int(word), 1);
-        *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = e;
-    }
     const int m0 = tc.m_block * p.kBlockM;
     const int rows_valid = min(p.kBlockM, p.rows - m0);
 
@@ -123,31 +125,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sm_l = reinterpret_cast<float*>(smem + C::kOffL);
     int* sm_diag = reinterpret_cast<int*>(smem + C::kOffDiag);
     const uint32_t bars = sbase + C::kOffBars;
-    auto bar_full = [&](int s) { return bars + 8u * s; };
-    auto bar_empty = [&](int s) { return bars + 8u * (ST + s); };
-    auto bar_sfull = [&](int i) { return bars + 8u * (2 * ST + i); };
-    auto bar_sempty = [&](int i) { return bars + 8u * (2 * ST + 2 + i); };
-    const uint32_t bar_pfull = bars + 8u * (2 * ST + 4);
-    const uint32_t bar_odone = bars + 8u * (2 * ST + 5);
-    const uint32_t bar_qfull = bars + 8u * (2 * ST + 6);
-    const uint32_t bar_never = bars + 8u * (2 * ST + 7);
-    const uint32_t bar_drain = bars + 8u * (2 * ST + 8);
+    // barriers: kfull[ST] kempty[ST] vfull[ST] vempty[ST] sfull[2] sempty[2] pfull[2] odone[2] q never drain
+    auto bar_kfull = [&](int s) { return bars + 8u * s; };
+    auto bar_kempty = [&](int s) { return bars + 8u * (ST + s); };
+    auto bar_vfull = [&](int s) { return bars + 8u * (2 * ST + s); };
+    auto bar_vempty = [&](int s) { return bars + 8u * (3 * ST + s); };
+    auto bar_sfull = [&](int i) { return bars + 8u * (4 * ST + i); };
+    auto bar_sempty = [&](int i) { return bars + 8u * (4 * ST + 2 + i); };
+    auto bar_pfull = [&](int i) { return bars + 8u * (4 * ST + 4 + i); };
+    auto bar_odone = [&](int i) { return bars + 8u * (4 * ST + 6 + i); };
+    const uint32_t bar_qfull = bars + 8u * (4 * ST + 8);
+    const uint32_t bar_never = bars + 8u * (4 * ST + 9);
+    const uint32_t bar_drain = bars + 8u * (4 * ST + 10);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-    auto stage_k = [&](int s) { return sbase + C::kOffStages + uint32_t(s) * C::kStageBytes; };
-    auto stage_v = [&](int s) { return stage_k(s) + C::kKBytes; };
+    auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
+    auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
-            mbar_init(bar_full(s), 1);
-            mbar_init(bar_empty(s), 1);
+            mbar_init(bar_kfull(s), 1);
+            mbar_init(bar_kempty(s), 1);
+            mbar_init(bar_vfull(s), 1);
+            mbar_init(bar_vempty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull(i), 1);
             mbar_init(bar_sempty(i), 128);
         }
-        mbar_init(bar_pfull, 128);
-        mbar_init(bar_odone, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_pfull(i), 128);
+            mbar_init(bar_odone(i), 1);
+        }
         mbar_init(bar_qfull, 128);
         mbar_init(bar_never, 1);
         mbar_init(bar_drain, 1);
@@ -165,34 +174,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touched only shared memory, TMEM and kernel parameters.
+    // Under programmatic dependent launch this grid may start while the previous
+    // kernel on the stream is still running: wait for it before any global access.
+    griddep_wait();
+    if (p.echo_plan && threadIdx.x == 0)
+        *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = make_int4(br.lo, br.hi, int(word), 1);
     const uint32_t tmem = *tmem_holder;
     const uint32_t tS0 = tmem;           // S^T buffers: columns [0, NP), [NP, 2NP)
     const uint32_t tO = tmem + 2 * NP;   // O^T: columns [2NP, 3NP)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
-        // ===================== TMA producer
+        // ===================== TMA producer (K and V rings)
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int j = 0; j < nblocks; ++j) {
-                const int s = j % ST;
-                const int u = j / ST;
-                if (u >= 1 && !mbar_wait(bar_empty(s), (u - 1) & 1, wc, (kKernDecode << 8) | kSiteProducerEmpty))
-                    break;
-                mbar_arrive_expect_tx(bar_full(s), 2 * C::kVLoadBytes);
-                const int y = kv_off + (br.lo + j) * 128;
-                const int kvh = p.pack_gqa ? ht : ht / p.G;
-#pragma unroll
-                for (int c = 0; c < HD / 64; ++c) {
-                    tma_load_2d(stage_k(s) + c * 16384, &tmK, bar_full(s), kvh * HD + c * 64, y, pol);
-                    tma_load_2d(stage_v(s) + c * 16384, &tmV, bar_full(s), kvh * HD + c * 64, y, pol);
-                }
-                issued = j + 1;
-            }
-            // Drain: the last load of every stage must land before the CTA exits.
-            for (int j = issued - 1; j >= 0 && j >= issued - ST; --j)
-                mbar_drain(bar_full(j % ST), (j / ST) & 1, p.timeout_ns);
+            const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
+            const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
+            const int kvh = p.pack_gqa ? ht : ht / p.G;
+            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, l2_policy_evict_first(), wc,
+                           (kKernDecode << 8) | kSiteProducerEmpty);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer
@@ -205,23 +205,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nblocks > 0)
                 ok = mbar_wait(bar_qfull, 0, wc, (kKernDecode << 8) | kSiteMmaQ) && ok;
             auto issue_pv = [&](int jj) {
-                bool good = mbar_wait(bar_pfull, jj & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
+                bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
+                tc_fence_after();
+                const int s = jj % ST;
+                good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull) && good;
                 tc_fence_after();
                 if (good) {
-                    const int s = jj % ST;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t a = make_sdesc_sw128(stage_v(s) + kk * 2048, 16384, 1024);
-                        const uint64_t bd = make_sdesc_sw128(sP + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = make_sdesc_sw128(sP + (jj & 1) * C::kPBuf + (kk >> 2) * (NP * 128) +
+                                                                 (kk & 3) * 32, 16, 1024);
                         umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(bar_odone);
-                    umma_commit(bar_empty(s));
+                    umma_commit(bar_odone(jj & 1));
+                    umma_commit(bar_vempty(s));
                 }
             };
             for (int j = 0; j < nblocks; ++j) {
                 const int s = j % ST;
-                bool good = mbar_wait(bar_full(s), (j / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
+                bool good = mbar_wait(bar_kfull(s), (j / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
                 if (j >= 2)
                     good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
                                      (kKernDecode << 8) | kSiteMmaSEmpty) && good;
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(bar_sfull(j & 1));
+                    umma_commit(bar_kempty(s));
                 }
                 if (j >= 1) issue_pv(j - 1);
             }
@@ -339,26 +343,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_t[q] += pv;
                 x[q] = pv;
             }
-            // PV of the previous block must be done before P and O are touched.
-            if (j >= 1) {
-                mbar_wait(bar_odone, (j - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+            // Rescaling O needs the previous block's PV to be complete.
+            if (need_all && j >= 1) {
+                mbar_wait(bar_odone((j - 1) & 1), ((j - 1) >> 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
-                if (need_all) {
 #pragma unroll
-                    for (int c = 0; c < NP / 16; ++c) {
-                        float o[16];
-                        tmem_ld16(tO + lane_off + c * 16, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < NP / 16; ++c) {
+                    float o[16];
+                    tmem_ld16(tO + lane_off + c * 16, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
-                        tmem_st16(tO + lane_off + c * 16, o);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
+                    tmem_st16(tO + lane_off + c * 16, o);
                 }
+                tmem_wait_st();
+            }
+            // P buffer (j & 1) was last read by the PV of block j - 2.
+            if (j >= 2) {
+                mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+                tc_fence_after();
             }
             // P^T[q][kt] (bf16) -> smem, K-major over keys, 128B swizzle.
             {
-                const uint32_t base = sP + (kt >> 6) * (NP * 128);
+                const uint32_t base = sP + (j & 1) * C::kPBuf + (kt >> 6) * (NP * 128);
                 const int g = (kt & 63) >> 3;
                 const uint32_t within = (kt & 7) * 2;
 #pragma unroll
@@ -372,9 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_pfull);
+            mbar_arrive(bar_pfull(j & 1));
         }
 
+        // Let the dependent grid (the combine, or the next call's partial kernel)
+        // get scheduled; it waits for this grid's completion before reading.
+        griddep_launch_dependents();
         // ---- epilogue: l across the 128 key lanes, then O^T / l
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -389,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < NP; ++q) o[q] = 0.f;
         if (nblocks >= 1) {
-            mbar_wait(bar_odone, (nblocks - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+            mbar_wait(bar_odone((nblocks - 1) & 1), ((nblocks - 1) >> 1) & 1, wc,
+                      (kKernDecode << 8) | kSiteSoftmaxODone);
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < NP / 16; ++c) tmem_ld16(tO + lane_off + c * 16, o + c * 16);
@@ -434,8 +445,8 @@ cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& 
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    kern<<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tmK, tmV, seqs);
-    return cudaGetLastError();
+    return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmK, tmV,
+                      seqs);
 }
 
 template <int HD, class Seqs>

@@ -15,12 +15,14 @@
 #include <math.h>
 
 #include "fwd_common.cuh"
+#include "kv_producer.cuh"
 #include "sm103_ptx.cuh"
 
 namespace sk {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;            // producer warp, MMA warp, 8 softmax warps
+constexpr int kSoftmaxThreads = 256;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -37,15 +39,22 @@ struct PrefillCfg {
     static constexpr int kVBytes = 128 * HD * 2;
     static constexpr int kStageBytes = kKBytes + kVBytes;
     static constexpr int kQBytes = 128 * HD * 2;
-    static constexpr int kPBytes = 128 * 128 * 2;
+    static constexpr int kPBuf = 128 * 128 * 2;   // one P buffer (bf16)
+    static constexpr int kPBytes = 2 * kPBuf;        // double-buffered
     static constexpr int kOffQ = 0;
-    static constexpr int kOffStages = kOffQ + kQBytes;
-    static constexpr int kOffP = kOffStages + kStages * kStageBytes;
-    static constexpr int kOffBars = kOffP + kPBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1 + 1 + 1;
+    static constexpr int kOffK = kOffQ + kQBytes;             // K ring: kStages slots
+    static constexpr int kOffV = kOffK + kStages * kKBytes;   // V ring: kStages slots
+    static constexpr int kOffP = kOffV + kStages * kVBytes;
+    static constexpr int kOffXchg = kOffP + kPBytes;       // float [2 slots][2 halves][128 rows]
+    static constexpr int kOffBars = kOffXchg + 2 * 2 * 128 * 4;
+    static constexpr int kNumBars = 4 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16;
-    static constexpr int kSmemAlloc = kSmemBytes + 1024;
+    // 1024 bytes of slack let the kernel align the operand base itself; when the
+    // budget has no room for it the kernel instead checks that the dynamic
+    // shared-memory base is already 1024-byte aligned.
+    static constexpr int kSlack = (kSmemBytes + 1024 <= 232448) ? 1024 : 0;
+    static constexpr int kSmemAlloc = kSmemBytes + kSlack;
     static constexpr int kTmemCols = 512;  // S0, S1 (128 columns each), O (HD columns)
     static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
@@ -56,7 +65,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Seqs seqs) {
     using C = PrefillCfg<HD>;
     constexpr int ST = C::kStages;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+        // No room to realign: report and leave before touching shared memory.
+        if (threadIdx.x == 0) atomicCAS(p.status, 0u, (kKernPrefill << 8) | kSiteSmemAlign);
+        return;
+    }
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -70,6 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long cta_lin =
         blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
     if (tc.split >= sb) {
+        griddep_launch_dependents();
+        griddep_wait();
         if (p.echo_plan && threadIdx.x == 0)
             *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = make_int4(0, 0, int(word), 0);
         return;
@@ -79,8 +95,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BlockRange br =
         n_block_range(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.flags, p.pack_gqa != 0, p.G, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
-    if (p.echo_plan && threadIdx.x == 0)
-        *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = make_int4(br.lo, br.hi, int(word), 1);
     const int m0 = tc.m_block * 128;
     const int rows_valid = min(128, p.rows - m0);
 
@@ -88,32 +102,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = sbase + C::kOffQ;
     const uint32_t sP = sbase + C::kOffP;
     const uint32_t bars = sbase + C::kOffBars;
-    auto bar_full = [&](int s) { return bars + 8u * s; };
-    auto bar_empty = [&](int s) { return bars + 8u * (ST + s); };
-    auto bar_sfull = [&](int i) { return bars + 8u * (2 * ST + i); };
-    auto bar_sempty = [&](int i) { return bars + 8u * (2 * ST + 2 + i); };
-    const uint32_t bar_pfull = bars + 8u * (2 * ST + 4);
-    const uint32_t bar_odone = bars + 8u * (2 * ST + 5);
-    const uint32_t bar_qfull = bars + 8u * (2 * ST + 6);
-    const uint32_t bar_never = bars + 8u * (2 * ST + 7);
-    const uint32_t bar_drain = bars + 8u * (2 * ST + 8);
+    // barriers: kfull[ST] kempty[ST] vfull[ST] vempty[ST] sfull[2] sempty[2] pfull[2] odone[2] q never drain
+    auto bar_kfull = [&](int s) { return bars + 8u * s; };
+    auto bar_kempty = [&](int s) { return bars + 8u * (ST + s); };
+    auto bar_vfull = [&](int s) { return bars + 8u * (2 * ST + s); };
+    auto bar_vempty = [&](int s) { return bars + 8u * (3 * ST + s); };
+    auto bar_sfull = [&](int i) { return bars + 8u * (4 * ST + i); };
+    auto bar_sempty = [&](int i) { return bars + 8u * (4 * ST + 2 + i); };
+    auto bar_pfull = [&](int i) { return bars + 8u * (4 * ST + 4 + i); };
+    auto bar_odone = [&](int i) { return bars + 8u * (4 * ST + 6 + i); };
+    const uint32_t bar_qfull = bars + 8u * (4 * ST + 8);
+    const uint32_t bar_never = bars + 8u * (4 * ST + 9);
+    const uint32_t bar_drain = bars + 8u * (4 * ST + 10);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-    auto stage_k = [&](int s) { return sbase + C::kOffStages + uint32_t(s) * C::kStageBytes; };
-    auto stage_v = [&](int s) { return stage_k(s) + C::kKBytes; };
+    auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
+    auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
-            mbar_init(bar_full(s), 1);
-            mbar_init(bar_empty(s), 1);
+            mbar_init(bar_kfull(s), 1);
+            mbar_init(bar_kempty(s), 1);
+            mbar_init(bar_vfull(s), 1);
+            mbar_init(bar_vempty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull(i), 1);
-            mbar_init(bar_sempty(i), 128);
+            mbar_init(bar_sempty(i), kSoftmaxThreads);
         }
-        mbar_init(bar_pfull, 128);
-        mbar_init(bar_odone, 1);
-        mbar_init(bar_qfull, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_pfull(i), kSoftmaxThreads);
+            mbar_init(bar_odone(i), 1);
+        }
+        mbar_init(bar_qfull, kSoftmaxThreads);
         mbar_init(bar_never, 1);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -130,6 +151,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touched only shared memory, TMEM and kernel parameters.
+    // Under programmatic dependent launch this grid may start while the previous
+    // kernel on the stream is still running: wait for it before any global access.
+    griddep_wait();
+    if (p.echo_plan && threadIdx.x == 0)
+        *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = make_int4(br.lo, br.hi, int(word), 1);
     const uint32_t tmem = *tmem_holder;
     const uint32_t tS0 = tmem;        // columns [0,128) and [128,256)
     const uint32_t tO = tmem + 256;   // columns [256, 256 + HD)
@@ -138,25 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // K/V of one head are re-read by the other m blocks: keep them in L2.
-            const uint64_t pol = l2_policy_evict_last();
-            int issued = 0;
-            for (int j = 0; j < nblocks; ++j) {
-                const int s = j % ST;
-                const int u = j / ST;
-                if (u >= 1 && !mbar_wait(bar_empty(s), (u - 1) & 1, wc, (kKernPrefill << 8) | kSiteProducerEmpty))
-                    break;
-                mbar_arrive_expect_tx(bar_full(s), C::kKBytes + C::kVBytes);
-                const int y = kv_off + (br.lo + j) * 128;
-                const int kvh = p.pack_gqa ? ht : ht / p.G;
-#pragma unroll
-                for (int c = 0; c < HD / 64; ++c) {
-                    tma_load_2d(stage_k(s) + c * 16384, &tmK, bar_full(s), kvh * HD + c * 64, y, pol);
-                    tma_load_2d(stage_v(s) + c * 16384, &tmV, bar_full(s), kvh * HD + c * 64, y, pol);
-                }
-                issued = j + 1;
-            }
-            for (int j = issued - 1; j >= 0 && j >= issued - ST; --j)
-                mbar_drain(bar_full(j % ST), (j / ST) & 1, p.timeout_ns);
+            const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
+            const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
+            const int kvh = p.pack_gqa ? ht : ht / p.G;
+            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, l2_policy_evict_last(), wc,
+                           (kKernPrefill << 8) | kSiteProducerEmpty);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -166,23 +179,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.inject_stall) ok = mbar_wait(bar_never, 0, wc, (kKernPrefill << 8) | kSiteInjected);
             if (nblocks > 0) ok = mbar_wait(bar_qfull, 0, wc, (kKernPrefill << 8) | kSiteMmaQ) && ok;
             auto issue_pv = [&](int jj) {
-                const bool good = mbar_wait(bar_pfull, jj & 1, wc, (kKernPrefill << 8) | kSiteMmaPFull);
+                const int s = jj % ST;
+                bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernPrefill << 8) | kSiteMmaPFull);
+                good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull) && good;
                 tc_fence_after();
                 if (good) {
-                    const int s = jj % ST;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = make_sdesc_sw128(sP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t a =
+                            make_sdesc_sw128(sP + (jj & 1) * C::kPBuf + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                         const uint64_t bd = make_sdesc_sw128(stage_v(s) + kk * 2048, 16384, 1024);
                         umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(bar_odone);
-                    umma_commit(bar_empty(s));
+                    umma_commit(bar_odone(jj & 1));
+                    umma_commit(bar_vempty(s));
                 }
             };
             for (int j = 0; j < nblocks; ++j) {
                 const int s = j % ST;
-                bool good = mbar_wait(bar_full(s), (j / ST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull);
+                bool good = mbar_wait(bar_kfull(s), (j / ST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull);
                 if (j >= 2)
                     good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
                                      (kKernPrefill << 8) | kSiteMmaSEmpty) && good;
@@ -195,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_bf16(tS0 + (j & 1) * 128, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(bar_sfull(j & 1));
+                    umma_commit(bar_kempty(s));
                 }
                 if (j >= 1) issue_pv(j - 1);
             }
@@ -203,13 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(bar_drain, 0, p.timeout_ns);
         }
     } else {
-        const int sidx = threadIdx.x - 64;
-        const int r = 32 * (warp & 3) + lane;  // query row of the tile = TMEM lane
+        // Softmax warps 2..9: two warpgroups, each owning 64 of the 128 key
+        // columns of every row (warps w and w + 4 share TMEM lane quadrant w % 4).
+        const int sidx = threadIdx.x - 64;                 // 0..255
+        const int half = (warp - 2) >> 2;                  // which 64 columns
+        const int r = 32 * (warp & 3) + lane;              // query row of the tile = TMEM lane
         const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+        float* xchg = reinterpret_cast<float*>(smem + C::kOffXchg);  // [slot][half][row]
 
-        // Q tile -> smem, K-major 128B swizzle (granule g of row r at sw128_offset).
+        // Q tile -> smem, K-major 128B swizzle (granule g of row rr at sw128_offset).
         constexpr int kGran = HD / 8;
-        for (int idx = sidx; idx < 128 * kGran; idx += 128) {
+        for (int idx = sidx; idx < 128 * kGran; idx += kSoftmaxThreads) {
             const int rr = idx / kGran;
             const int g16 = idx - rr * kGran;
             uint4 val = make_uint4(0, 0, 0, 0);
@@ -237,16 +257,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_causal = p.causal != 0;
         const bool has_window = p.window_left >= 0;
         const float sl2 = p.scale_log2;
+        const int col0 = half * 64;
 
-        float m_run = -INFINITY;  // running max, log2 units (scaled)
-        float l_run = 0.f;
+        float m_run = -INFINITY;  // running row max, log2 units (scaled); same in both halves
+        float l_run = 0.f;        // this half's share of the row sum
         for (int j = 0; j < nblocks; ++j) {
             const int n = br.lo + j;
-            float x[128];
+            float x[64];
             mbar_wait(bar_sfull(j & 1), (j >> 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxSFull);
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 8; ++c) tmem_ld16(tS0 + (j & 1) * 128 + lane_off + c * 16, x + c * 16);
+            for (int c = 0; c < 4; ++c) tmem_ld16(tS0 + (j & 1) * 128 + col0 + lane_off + c * 16, x + c * 16);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar_sempty(j & 1));
@@ -256,16 +277,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    (has_window && blk_first < diag_hi - p.window_left) || rows_valid < 128;
             if (need_mask) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = blk_first + c;
+                for (int c = 0; c < 64; ++c) {
+                    const int key = blk_first + col0 + c;
                     const bool vis = row_ok && key < sk && !(has_causal && key > diag) &&
                                      !(has_window && key < diag - p.window_left);
                     if (!vis) x[c] = -INFINITY;
                 }
             }
-            float mx = x[0];
+            float mx8[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            for (int c = 0; c < 8; ++c) mx8[c] = x[c];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // row max = max over both halves (double-buffered exchange slot)
+            xchg[((j & 1) * 2 + half) * 128 + r] = mx;
+            named_bar_sync(1, kSoftmaxThreads);
+            mx = fmaxf(mx, xchg[((j & 1) * 2 + (half ^ 1)) * 128 + r]);
             const float cand = mx * sl2;
             bool rescale = false;
             float alpha = 1.f;
@@ -276,77 +305,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = cand;
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-            float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                x[c + 0] = fast_exp2(fmaf(x[c + 0], sl2, neg_m));
-                x[c + 1] = fast_exp2(fmaf(x[c + 1], sl2, neg_m));
-                x[c + 2] = fast_exp2(fmaf(x[c + 2], sl2, neg_m));
-                x[c + 3] = fast_exp2(fmaf(x[c + 3], sl2, neg_m));
-                ls0 += x[c + 0];
-                ls1 += x[c + 1];
-                ls2 += x[c + 2];
-                ls3 += x[c + 3];
+            for (int c = 0; c < 64; ++c) {
+                x[c] = fast_exp2(fmaf(x[c], sl2, neg_m));
+                ls[c & 3] += x[c];
             }
-            l_run += (ls0 + ls1) + (ls2 + ls3);
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
-            if (j >= 1) {
-                mbar_wait(bar_odone, (j - 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
-                tc_fence_after();
-            }
-            // Each row rescales its own TMEM lane.  tcgen05.ld/st are warp-collective
-            // (.sync.aligned), so the whole warp enters together; rows that keep
-            // their max multiply by 1.
+            // Each row rescales its own TMEM lane (this half's HD/2 columns) once
+            // the previous PV is done.  tcgen05.ld/st are warp-collective
+            // (.sync.aligned): the whole warp enters; rows that keep their max x 1.
             if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                mbar_wait(bar_odone((j - 1) & 1), ((j - 1) >> 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
+                tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < HD / 16; ++c) {
+                for (int c = 0; c < HD / 32; ++c) {
                     float o[16];
-                    tmem_ld16(tO + lane_off + c * 16, o);
+                    const uint32_t ta = tO + half * (HD / 2) + lane_off + c * 16;
+                    tmem_ld16(ta, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) o[e] *= a;
-                    tmem_st16(tO + lane_off + c * 16, o);
+                    tmem_st16(ta, o);
                 }
                 tmem_wait_st();
             }
-            // P row (bf16) -> smem, K-major over keys, 128B swizzle.
+            // P buffer (j & 1) was last read by the PV of block j - 2.
+            if (j >= 2) {
+                mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
+                tc_fence_after();
+            }
+            // This half's 64 keys of the P row (bf16) -> smem chunk `half`, 128B swizzle.
 #pragma unroll
-            for (int g16 = 0; g16 < 16; ++g16) {
-                const uint32_t w0 = pack_bf16x2(x[g16 * 8 + 0], x[g16 * 8 + 1]);
-                const uint32_t w1 = pack_bf16x2(x[g16 * 8 + 2], x[g16 * 8 + 3]);
-                const uint32_t w2 = pack_bf16x2(x[g16 * 8 + 4], x[g16 * 8 + 5]);
-                const uint32_t w3 = pack_bf16x2(x[g16 * 8 + 6], x[g16 * 8 + 7]);
-                const uint32_t dst = sP + (g16 >> 3) * 16384 + sw128_offset(r, g16 & 7);
+            for (int g = 0; g < 8; ++g) {
+                const uint32_t w0 = pack_bf16x2(x[g * 8 + 0], x[g * 8 + 1]);
+                const uint32_t w1 = pack_bf16x2(x[g * 8 + 2], x[g * 8 + 3]);
+                const uint32_t w2 = pack_bf16x2(x[g * 8 + 4], x[g * 8 + 5]);
+                const uint32_t w3 = pack_bf16x2(x[g * 8 + 6], x[g * 8 + 7]);
+                const uint32_t dst = sP + (j & 1) * C::kPBuf + half * 16384 + sw128_offset(r, g);
                 asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w0), "r"(w1),
                              "r"(w2), "r"(w3)
                              : "memory");
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_pfull);
+            mbar_arrive(bar_pfull(j & 1));
         }
 
-        // ---- epilogue
+        // Let the dependent grid (the combine, or the next call's partial kernel)
+        // get scheduled; it waits for this grid's completion before reading.
+        griddep_launch_dependents();
+        // ---- epilogue: row sum over both halves, O / l, this half's HD/2 columns
+        xchg[half * 128 + r] = l_run;
+        named_bar_sync(1, kSoftmaxThreads);
+        const float l_tot = l_run + xchg[(half ^ 1) * 128 + r];
         if (nblocks >= 1) {
-            mbar_wait(bar_odone, (nblocks - 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
+            mbar_wait(bar_odone((nblocks - 1) & 1), ((nblocks - 1) >> 1) & 1, wc,
+                      (kKernPrefill << 8) | kSiteSoftmaxODone);
             tc_fence_after();
         }
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        const float lse = l_tot > 0.f ? (m_run + log2f(l_tot)) * kLn2 : -INFINITY;
         const bool final_out = (sb == 1);
 #pragma unroll
-        for (int c = 0; c < HD / 16; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
             float o[16];
             if (nblocks >= 1) {
-                tmem_ld16(tO + lane_off + c * 16, o);
+                tmem_ld16(tO + half * (HD / 2) + lane_off + c * 16, o);
                 tmem_wait_ld();
             }
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = (nblocks >= 1 && l_run > 0.f) ? o[e] * inv : 0.f;
+            for (int e = 0; e < 16; ++e) o[e] = (nblocks >= 1 && l_tot > 0.f) ? o[e] * inv : 0.f;
+            const int dcol = half * (HD / 2) + c * 16;
             if (row_ok) {
                 if (final_out) {
-                    __nv_bfloat16* dst = p.out + ((size_t(b) * p.sq + my.i) * p.Hq + my.h) * HD + c * 16;
+                    __nv_bfloat16* dst = p.out + ((size_t(b) * p.sq + my.i) * p.Hq + my.h) * HD + dcol;
                     uint4 w0, w1;
                     w0.x = pack_bf16x2(o[0], o[1]); w0.y = pack_bf16x2(o[2], o[3]);
                     w0.z = pack_bf16x2(o[4], o[5]); w0.w = pack_bf16x2(o[6], o[7]);
@@ -356,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     reinterpret_cast<uint4*>(dst)[1] = w1;
                 } else {
                     const size_t prow = ((size_t(tc.split) * p.B + b) * p.Hq + my.h) * p.sq + my.i;
-                    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * HD + c * 16);
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * HD + dcol);
                     dst[0] = make_float4(o[0], o[1], o[2], o[3]);
                     dst[1] = make_float4(o[4], o[5], o[6], o[7]);
                     dst[2] = make_float4(o[8], o[9], o[10], o[11]);
@@ -364,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (row_ok) {
+        if (row_ok && half == 0) {
             if (final_out)
                 p.lse[(size_t(b) * p.Hq + my.h) * p.sq + my.i] = lse;
             else
@@ -389,8 +424,8 @@ cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& 
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    kern<<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tmK, tmV, seqs);
-    return cudaGetLastError();
+    return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmK, tmV,
+                      seqs);
 }
 
 }  // namespace

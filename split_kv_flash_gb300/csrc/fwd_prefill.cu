@@ -34,20 +34,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 template <int HD>
 struct PrefillCfg {
-    static constexpr int kStages = HD == 128 ? 2 : 4;
+    // P lives in TMEM (A operand of the PV MMA), which leaves room for a third K slot.
+    static constexpr int kStagesK = HD == 128 ? 3 : 4;
+    static constexpr int kStagesV = HD == 128 ? 3 : 4;
     static constexpr int kKBytes = 128 * HD * 2;
     static constexpr int kVBytes = 128 * HD * 2;
     static constexpr int kStageBytes = kKBytes + kVBytes;
     static constexpr int kQBytes = 128 * HD * 2;
-    static constexpr int kPBuf = 128 * 128 * 2;   // one P buffer (bf16)
-    static constexpr int kPBytes = 2 * kPBuf;        // double-buffered
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;             // K ring: kStages slots
-    static constexpr int kOffV = kOffK + kStages * kKBytes;   // V ring: kStages slots
-    static constexpr int kOffP = kOffV + kStages * kVBytes;
-    static constexpr int kOffXchg = kOffP + kPBytes;       // float [2 slots][2 halves][128 rows]
+    static constexpr int kOffK = kOffQ + kQBytes;              // K ring: kStagesK slots
+    static constexpr int kOffV = kOffK + kStagesK * kKBytes;   // V ring: kStagesV slots
+    static constexpr int kOffXchg = kOffV + kStagesV * kVBytes;  // float [2 slots][2 halves][128 rows]
     static constexpr int kOffBars = kOffXchg + 2 * 2 * 128 * 4;
-    static constexpr int kNumBars = 4 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+    static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 1 + 1;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16;
     // 1024 bytes of slack let the kernel align the operand base itself; when the
@@ -55,7 +54,9 @@ struct PrefillCfg {
     // shared-memory base is already 1024-byte aligned.
     static constexpr int kSlack = (kSmemBytes + 1024 <= 232448) ? 1024 : 0;
     static constexpr int kSmemAlloc = kSmemBytes + kSlack;
-    static constexpr int kTmemCols = 512;  // S0, S1 (128 columns each), O (HD columns)
+    // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+HD), P0 [384,448), P1 [448,512)
+    // (P: 128 keys as 64 columns of packed bf16 pairs).
+    static constexpr int kTmemCols = 512;
     static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
 
@@ -64,7 +65,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_prefill_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Seqs seqs) {
     using C = PrefillCfg<HD>;
-    constexpr int ST = C::kStages;
+    constexpr int KST = C::kStagesK;
+    constexpr int VST = C::kStagesV;
+    constexpr int NB0 = 2 * KST + 2 * VST;  // first barrier after the rings
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
         // No room to realign: report and leave before touching shared memory.
@@ -100,29 +103,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::kOffQ;
-    const uint32_t sP = sbase + C::kOffP;
     const uint32_t bars = sbase + C::kOffBars;
-    // barriers: kfull[ST] kempty[ST] vfull[ST] vempty[ST] sfull[2] sempty[2] pfull[2] odone[2] q never drain
+    // barriers: kfull[KST] kempty[KST] vfull[VST] vempty[VST] sfull[2] sempty[2] pfull[2] odone[2] q never drain
     auto bar_kfull = [&](int s) { return bars + 8u * s; };
-    auto bar_kempty = [&](int s) { return bars + 8u * (ST + s); };
-    auto bar_vfull = [&](int s) { return bars + 8u * (2 * ST + s); };
-    auto bar_vempty = [&](int s) { return bars + 8u * (3 * ST + s); };
-    auto bar_sfull = [&](int i) { return bars + 8u * (4 * ST + i); };
-    auto bar_sempty = [&](int i) { return bars + 8u * (4 * ST + 2 + i); };
-    auto bar_pfull = [&](int i) { return bars + 8u * (4 * ST + 4 + i); };
-    auto bar_odone = [&](int i) { return bars + 8u * (4 * ST + 6 + i); };
-    const uint32_t bar_qfull = bars + 8u * (4 * ST + 8);
-    const uint32_t bar_never = bars + 8u * (4 * ST + 9);
-    const uint32_t bar_drain = bars + 8u * (4 * ST + 10);
+    auto bar_kempty = [&](int s) { return bars + 8u * (KST + s); };
+    auto bar_vfull = [&](int s) { return bars + 8u * (2 * KST + s); };
+    auto bar_vempty = [&](int s) { return bars + 8u * (2 * KST + VST + s); };
+    auto bar_sfull = [&](int i) { return bars + 8u * (NB0 + i); };
+    auto bar_sempty = [&](int i) { return bars + 8u * (NB0 + 2 + i); };
+    auto bar_pfull = [&](int i) { return bars + 8u * (NB0 + 4 + i); };
+    auto bar_odone = [&](int i) { return bars + 8u * (NB0 + 6 + i); };
+    const uint32_t bar_qfull = bars + 8u * (NB0 + 8);
+    const uint32_t bar_never = bars + 8u * (NB0 + 9);
+    const uint32_t bar_drain = bars + 8u * (NB0 + 10);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
     auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(bar_kfull(s), 1);
             mbar_init(bar_kempty(s), 1);
+        }
+        for (int s = 0; s < VST; ++s) {
             mbar_init(bar_vfull(s), 1);
             mbar_init(bar_vempty(s), 1);
         }
@@ -160,13 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const uint32_t tS0 = tmem;        // columns [0,128) and [128,256)
     const uint32_t tO = tmem + 256;   // columns [256, 256 + HD)
+    const uint32_t tP0 = tmem + 384;  // P buffers: columns [384, 448) and [448, 512)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
         if (lane == 0) {
             // K/V of one head are re-read by the other m blocks: keep them in L2.
-            const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
-            const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
+            const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
+            const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
             const int kvh = p.pack_gqa ? ht : ht / p.G;
             produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, l2_policy_evict_last(), wc,
                            (kKernPrefill << 8) | kSiteProducerEmpty);
@@ -179,25 +184,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.inject_stall) ok = mbar_wait(bar_never, 0, wc, (kKernPrefill << 8) | kSiteInjected);
             if (nblocks > 0) ok = mbar_wait(bar_qfull, 0, wc, (kKernPrefill << 8) | kSiteMmaQ) && ok;
             auto issue_pv = [&](int jj) {
-                const int s = jj % ST;
+                const int s = jj % VST;
                 bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernPrefill << 8) | kSiteMmaPFull);
-                good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull) && good;
+                good = mbar_wait(bar_vfull(s), (jj / VST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull) && good;
                 tc_fence_after();
                 if (good) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a =
-                            make_sdesc_sw128(sP + (jj & 1) * C::kPBuf + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        // A = P from TMEM: 16 keys = 8 packed columns per MMA.
                         const uint64_t bd = make_sdesc_sw128(stage_v(s) + kk * 2048, 16384, 1024);
-                        umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(tO, tP0 + (jj & 1) * 64 + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_odone(jj & 1));
                     umma_commit(bar_vempty(s));
                 }
             };
             for (int j = 0; j < nblocks; ++j) {
-                const int s = j % ST;
-                bool good = mbar_wait(bar_kfull(s), (j / ST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull);
+                const int s = j % KST;
+                bool good = mbar_wait(bar_kfull(s), (j / KST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull);
                 if (j >= 2)
                     good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
                                      (kKernPrefill << 8) | kSiteMmaSEmpty) && good;
@@ -332,24 +336,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // P buffer (j & 1) was last read by the PV of block j - 2.
+            // P buffer (j & 1) in TMEM was last read by the PV of block j - 2.
             if (j >= 2) {
                 mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
-            // This half's 64 keys of the P row (bf16) -> smem chunk `half`, 128B swizzle.
+            // This half's 64 keys of the P row -> TMEM: 32 columns of packed bf16 pairs.
+            {
+                uint32_t pk[32];
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const uint32_t w0 = pack_bf16x2(x[g * 8 + 0], x[g * 8 + 1]);
-                const uint32_t w1 = pack_bf16x2(x[g * 8 + 2], x[g * 8 + 3]);
-                const uint32_t w2 = pack_bf16x2(x[g * 8 + 4], x[g * 8 + 5]);
-                const uint32_t w3 = pack_bf16x2(x[g * 8 + 6], x[g * 8 + 7]);
-                const uint32_t dst = sP + (j & 1) * C::kPBuf + half * 16384 + sw128_offset(r, g);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w0), "r"(w1),
-                             "r"(w2), "r"(w3)
-                             : "memory");
+                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+                const uint32_t ta = tP0 + (j & 1) * 64 + half * 32 + lane_off;
+                tmem_st16u(ta, pk);
+                tmem_st16u(ta + 16, pk + 16);
+                tmem_wait_st();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar_pfull(j & 1));
         }

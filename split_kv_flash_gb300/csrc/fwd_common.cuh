@@ -97,17 +97,22 @@ void fill_varlen(const Plan& plan, VarlenSeqs* v);
 // (griddepcontrol.wait) before touching global memory.
 template <class Seqs>
 cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream,
-                       const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const Seqs& seqs) {
+                       const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const Seqs& seqs,
+                       int cluster_y = 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = unsigned(cluster_y);
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster_y > 1 ? 2 : 1;
     void* args[4] = {const_cast<FwdParams*>(&p), const_cast<CUtensorMap*>(&tmK), const_cast<CUtensorMap*>(&tmV),
                      const_cast<Seqs*>(&seqs)};
     return cudaLaunchKernelExC(&cfg, kernel, args);

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
             const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
             const int kvh = p.pack_gqa ? ht : ht / p.G;
-            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, l2_policy_evict_first(), wc,
+            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, 0, l2_policy_evict_first(), wc,
                            (kKernDecode << 8) | kSiteProducerEmpty);
         }
     } else if (warp == 1) {
@@ -253,21 +253,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
         const int diag_shift = sk - p.sq;
 
-        // Q tile -> smem (K-major, 128B swizzle), padded rows zero.
-        constexpr int kGran = HD / 8;  // 16-byte granules per row
-        for (int idx = sidx; idx < NP * kGran; idx += 128) {
-            const int r = idx / kGran;
-            const int g16 = idx - r * kGran;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (r < rows_valid) {
-                const RowMap rm = map_row(p, ht, m0 + r);
-                val = __ldg(reinterpret_cast<const uint4*>(
-                    p.q + ((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + g16 * 8));
+        // Q tile -> smem (K-major, 128B swizzle), padded rows zero.  All of a
+        // thread's loads are issued before any store so that they overlap.
+        {
+            constexpr int kGran = HD / 8;  // 16-byte granules per row
+            constexpr int kPer = (NP * kGran + 127) / 128;
+            uint4 val[kPer];
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                const int idx = sidx + t * 128;
+                const int r = idx / kGran;
+                const int g16 = idx - r * kGran;
+                val[t] = make_uint4(0, 0, 0, 0);
+                if (idx < NP * kGran && r < rows_valid) {
+                    const RowMap rm = map_row(p, ht, m0 + r);
+                    val[t] = __ldg(reinterpret_cast<const uint4*>(
+                        p.q + ((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + g16 * 8));
+                }
             }
-            const uint32_t dst = sQ + (g16 >> 3) * (NP * 128) + sw128_offset(r, g16 & 7);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val.x), "r"(val.y),
-                         "r"(val.z), "r"(val.w)
-                         : "memory");
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                const int idx = sidx + t * 128;
+                if (idx < NP * kGran) {
+                    const int r = idx / kGran;
+                    const int g16 = idx - r * kGran;
+                    const uint32_t dst = sQ + (g16 >> 3) * (NP * 128) + sw128_offset(r, g16 & 7);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val[t].x), "r"(val[t].y),
+                                 "r"(val[t].z), "r"(val[t].w)
+                                 : "memory");
+                }
+            }
         }
         if (sidx < NP) {
             sm_m[sidx] = -INFINITY;

@@ -21,8 +21,16 @@
 namespace sk {
 namespace {
 
-constexpr int kThreads = 320;            // producer warp, MMA warp, 8 softmax warps
-constexpr int kSoftmaxThreads = 256;
+// The 128 key columns of every row are split over kGroups softmax warpgroups
+// (warps w and w + 4 share TMEM lane quadrant w % 4): more warps per scheduler
+// hide the latency of the TMEM loads, the exp2 and the barriers.
+#ifndef SK_PREFILL_COLGROUPS
+#define SK_PREFILL_COLGROUPS 2
+#endif
+constexpr int kGroups = SK_PREFILL_COLGROUPS;
+constexpr int kSoftmaxThreads = 128 * kGroups;
+constexpr int kThreads = 64 + kSoftmaxThreads;  // producer warp, MMA warp, softmax warps
+constexpr int kCW = 128 / kGroups;              // S / P columns (keys) per thread
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -36,7 +44,7 @@ template <int HD>
 struct PrefillCfg {
     // P lives in TMEM (A operand of the PV MMA), which leaves room for a third K slot.
     static constexpr int kStagesK = HD == 128 ? 3 : 4;
-    static constexpr int kStagesV = HD == 128 ? 3 : 4;
+    static constexpr int kStagesV = HD == 128 ? (kGroups > 2 ? 2 : 3) : 4;
     static constexpr int kKBytes = 128 * HD * 2;
     static constexpr int kVBytes = 128 * HD * 2;
     static constexpr int kStageBytes = kKBytes + kVBytes;
@@ -44,8 +52,8 @@ struct PrefillCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;              // K ring: kStagesK slots
     static constexpr int kOffV = kOffK + kStagesK * kKBytes;   // V ring: kStagesV slots
-    static constexpr int kOffXchg = kOffV + kStagesV * kVBytes;  // float [2 slots][2 halves][128 rows]
-    static constexpr int kOffBars = kOffXchg + 2 * 2 * 128 * 4;
+    static constexpr int kOffXchg = kOffV + kStagesV * kVBytes;  // float [2 slots][kGroups][128 rows]
+    static constexpr int kOffBars = kOffXchg + 2 * kGroups * 128 * 4;
     static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 1 + 1;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16;
@@ -60,7 +68,9 @@ struct PrefillCfg {
     static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
 
-template <int HD, class Seqs>
+// PAIR: the CTA is one of a 2-CTA cluster (two query heads of one KV head with
+// identical block ranges) that share every K/V block through TMA multicast.
+template <int HD, class Seqs, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_prefill_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Seqs seqs) {
@@ -98,6 +108,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BlockRange br =
         n_block_range(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.flags, p.pack_gqa != 0, p.G, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
+    const int kvh = p.pack_gqa ? ht : ht / p.G;
+    // per-CTA starting block (spreads the CTAs of one KV head over its K/V; equal
+    // within a cluster pair, which shares the loads)
+    uint32_t hsh = uint32_t(tc.m_block) * 0x9E3779B1u + uint32_t(kvh) * 0x85EBCA77u + uint32_t(b) * 0xC2B2AE3Du;
+    hsh ^= hsh >> 15;
+    hsh *= 0x2C1B3C6Du;
+    hsh ^= hsh >> 12;
+    const int rot = nblocks > 0 ? int(hsh % uint32_t(nblocks)) : 0;
     const int m0 = tc.m_block * 128;
     const int rows_valid = min(128, p.rows - m0);
 
@@ -124,11 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < KST; ++s) {
             mbar_init(bar_kfull(s), 1);
-            mbar_init(bar_kempty(s), 1);
+            mbar_init(bar_kempty(s), PAIR ? 2 : 1);  // a paired slot is released by both CTAs
         }
         for (int s = 0; s < VST; ++s) {
             mbar_init(bar_vfull(s), 1);
-            mbar_init(bar_vempty(s), 1);
+            mbar_init(bar_vempty(s), PAIR ? 2 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sfull(i), 1);
@@ -154,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the partner's barriers are initialised before any multicast
     tc_fence_after();
     // Everything above touched only shared memory, TMEM and kernel parameters.
     // Under programmatic dependent launch this grid may start while the previous
@@ -172,9 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K/V of one head are re-read by the other m blocks: keep them in L2.
             const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
             const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
-            const int kvh = p.pack_gqa ? ht : ht / p.G;
-            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, l2_policy_evict_last(), wc,
-                           (kKernPrefill << 8) | kSiteProducerEmpty);
+            if constexpr (PAIR)
+                produce_kv_pair<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, rot,
+                                    cluster_ctarank(), l2_policy_evict_last(), wc,
+                                    (kKernPrefill << 8) | kSiteProducerEmpty);
+            else
+                produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, rot,
+                               l2_policy_evict_last(), wc, (kKernPrefill << 8) | kSiteProducerEmpty);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -196,7 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_bf16_ts(tO, tP0 + (jj & 1) * 64 + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_odone(jj & 1));
-                    umma_commit(bar_vempty(s));
+                    if constexpr (PAIR)
+                        umma_commit_mc(bar_vempty(s), uint16_t(0x3));
+                    else
+                        umma_commit(bar_vempty(s));
                 }
             };
             for (int j = 0; j < nblocks; ++j) {
@@ -214,7 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_bf16(tS0 + (j & 1) * 128, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(bar_sfull(j & 1));
-                    umma_commit(bar_kempty(s));
+                    if constexpr (PAIR)
+                        umma_commit_mc(bar_kempty(s), uint16_t(0x3));
+                    else
+                        umma_commit(bar_kempty(s));
                 }
                 if (j >= 1) issue_pv(j - 1);
             }
@@ -223,29 +252,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(bar_drain, 0, p.timeout_ns);
         }
     } else {
-        // Softmax warps 2..9: two warpgroups, each owning 64 of the 128 key
-        // columns of every row (warps w and w + 4 share TMEM lane quadrant w % 4).
-        const int sidx = threadIdx.x - 64;                 // 0..255
-        const int half = (warp - 2) >> 2;                  // which 64 columns
+        // Softmax warps 2..(2 + 4 * kGroups): group g owns key columns
+        // [g * kCW, (g + 1) * kCW) of every row and O columns [g * HD / kGroups, ...).
+        const int sidx = threadIdx.x - 64;                 // 0 .. kSoftmaxThreads - 1
+        const int grp = (warp - 2) >> 2;                   // column group
         const int r = 32 * (warp & 3) + lane;              // query row of the tile = TMEM lane
         const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-        float* xchg = reinterpret_cast<float*>(smem + C::kOffXchg);  // [slot][half][row]
+        float* xchg = reinterpret_cast<float*>(smem + C::kOffXchg);  // [slot][group][row]
+        constexpr int kOW = HD / kGroups;                  // O columns per thread
 
         // Q tile -> smem, K-major 128B swizzle (granule g of row rr at sw128_offset).
-        constexpr int kGran = HD / 8;
-        for (int idx = sidx; idx < 128 * kGran; idx += kSoftmaxThreads) {
-            const int rr = idx / kGran;
-            const int g16 = idx - rr * kGran;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (rr < rows_valid) {
-                const RowMap rm = map_row(p, ht, m0 + rr);
-                val = __ldg(reinterpret_cast<const uint4*>(
-                    p.q + ((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + g16 * 8));
+        // All of a thread's loads are issued before any store so that they overlap.
+        {
+            constexpr int kGran = HD / 8;
+            constexpr int kPer = 128 * kGran / kSoftmaxThreads;
+            uint4 val[kPer];
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                const int idx = sidx + t * kSoftmaxThreads;
+                const int rr = idx / kGran;
+                const int g16 = idx - rr * kGran;
+                val[t] = make_uint4(0, 0, 0, 0);
+                if (rr < rows_valid) {
+                    const RowMap rm = map_row(p, ht, m0 + rr);
+                    val[t] = __ldg(reinterpret_cast<const uint4*>(
+                        p.q + ((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + g16 * 8));
+                }
             }
-            const uint32_t dst = sQ + (g16 >> 3) * 16384 + sw128_offset(rr, g16 & 7);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val.x), "r"(val.y),
-                         "r"(val.z), "r"(val.w)
-                         : "memory");
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                const int idx = sidx + t * kSoftmaxThreads;
+                const int rr = idx / kGran;
+                const int g16 = idx - rr * kGran;
+                const uint32_t dst = sQ + (g16 >> 3) * 16384 + sw128_offset(rr, g16 & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val[t].x), "r"(val[t].y),
+                             "r"(val[t].z), "r"(val[t].w)
+                             : "memory");
+            }
         }
         fence_proxy_async_smem();
         mbar_arrive(bar_qfull);
@@ -261,17 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_causal = p.causal != 0;
         const bool has_window = p.window_left >= 0;
         const float sl2 = p.scale_log2;
-        const int col0 = half * 64;
+        const int col0 = grp * kCW;
 
-        float m_run = -INFINITY;  // running row max, log2 units (scaled); same in both halves
-        float l_run = 0.f;        // this half's share of the row sum
+        float m_run = -INFINITY;  // running row max, log2 units (scaled); same in every group
+        float l_run = 0.f;        // this group's share of the row sum
         for (int j = 0; j < nblocks; ++j) {
-            const int n = br.lo + j;
-            float x[64];
+            const int n = br.lo + rotated_block(j, rot, nblocks);
+            float x[kCW];
             mbar_wait(bar_sfull(j & 1), (j >> 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxSFull);
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld16(tS0 + (j & 1) * 128 + col0 + lane_off + c * 16, x + c * 16);
+            for (int c = 0; c < kCW / 16; ++c) tmem_ld16(tS0 + (j & 1) * 128 + col0 + lane_off + c * 16, x + c * 16);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar_sempty(j & 1));
@@ -281,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    (has_window && blk_first < diag_hi - p.window_left) || rows_valid < 128;
             if (need_mask) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < kCW; ++c) {
                     const int key = blk_first + col0 + c;
                     const bool vis = row_ok && key < sk && !(has_causal && key > diag) &&
                                      !(has_window && key < diag - p.window_left);
@@ -292,13 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 8; ++c) mx8[c] = x[c];
 #pragma unroll
-            for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+            for (int c = 8; c < kCW; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
             float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            // row max = max over both halves (double-buffered exchange slot)
-            xchg[((j & 1) * 2 + half) * 128 + r] = mx;
+            // row max over the groups (double-buffered exchange slot)
+            xchg[((j & 1) * kGroups + grp) * 128 + r] = mx;
             named_bar_sync(1, kSoftmaxThreads);
-            mx = fmaxf(mx, xchg[((j & 1) * 2 + (half ^ 1)) * 128 + r]);
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g)
+                if (g != grp) mx = fmaxf(mx, xchg[((j & 1) * kGroups + g) * 128 + r]);
             const float cand = mx * sl2;
             bool rescale = false;
             float alpha = 1.f;
@@ -311,13 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < kCW; ++c) {
                 x[c] = fast_exp2(fmaf(x[c], sl2, neg_m));
                 ls[c & 3] += x[c];
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
-            // Each row rescales its own TMEM lane (this half's HD/2 columns) once
+            // Each row rescales its own TMEM lane (this group's HD/kGroups columns) once
             // the previous PV is done.  tcgen05.ld/st are warp-collective
             // (.sync.aligned): the whole warp enters; rows that keep their max x 1.
             if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
@@ -325,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
+                for (int c = 0; c < kOW / 16; ++c) {
                     float o[16];
-                    const uint32_t ta = tO + half * (HD / 2) + lane_off + c * 16;
+                    const uint32_t ta = tO + grp * kOW + lane_off + c * 16;
                     tmem_ld16(ta, o);
                     tmem_wait_ld();
 #pragma unroll
@@ -341,14 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
-            // This half's 64 keys of the P row -> TMEM: 32 columns of packed bf16 pairs.
+            // This group's keys of the P row -> TMEM: kCW / 2 columns of packed bf16 pairs.
             {
-                uint32_t pk[32];
+                uint32_t pk[kCW / 2];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
-                const uint32_t ta = tP0 + (j & 1) * 64 + half * 32 + lane_off;
-                tmem_st16u(ta, pk);
-                tmem_st16u(ta + 16, pk + 16);
+                for (int c = 0; c < kCW / 2; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+                const uint32_t ta = tP0 + (j & 1) * 64 + grp * (kCW / 2) + lane_off;
+#pragma unroll
+                for (int c = 0; c < kCW / 32; ++c) tmem_st16u(ta + c * 16, pk + c * 16);
                 tmem_wait_st();
             }
             tc_fence_before();
@@ -358,10 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Let the dependent grid (the combine, or the next call's partial kernel)
         // get scheduled; it waits for this grid's completion before reading.
         griddep_launch_dependents();
-        // ---- epilogue: row sum over both halves, O / l, this half's HD/2 columns
-        xchg[half * 128 + r] = l_run;
+        // ---- epilogue: row sum over the groups, O / l, this group's HD/kGroups columns
+        xchg[grp * 128 + r] = l_run;
         named_bar_sync(1, kSoftmaxThreads);
-        const float l_tot = l_run + xchg[(half ^ 1) * 128 + r];
+        float l_tot = 0.f;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) l_tot += xchg[g * 128 + r];
         if (nblocks >= 1) {
             mbar_wait(bar_odone((nblocks - 1) & 1), ((nblocks - 1) >> 1) & 1, wc,
                       (kKernPrefill << 8) | kSiteSoftmaxODone);
@@ -371,15 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse = l_tot > 0.f ? (m_run + log2f(l_tot)) * kLn2 : -INFINITY;
         const bool final_out = (sb == 1);
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < kOW / 16; ++c) {
             float o[16];
             if (nblocks >= 1) {
-                tmem_ld16(tO + half * (HD / 2) + lane_off + c * 16, o);
+                tmem_ld16(tO + grp * kOW + lane_off + c * 16, o);
                 tmem_wait_ld();
             }
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] = (nblocks >= 1 && l_tot > 0.f) ? o[e] * inv : 0.f;
-            const int dcol = half * (HD / 2) + c * 16;
+            const int dcol = grp * kOW + c * 16;
             if (row_ok) {
                 if (final_out) {
                     __nv_bfloat16* dst = p.out + ((size_t(b) * p.sq + my.i) * p.Hq + my.h) * HD + dcol;
@@ -400,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (row_ok && half == 0) {
+        if (row_ok && grp == 0) {
             if (final_out)
                 p.lse[(size_t(b) * p.Hq + my.h) * p.sq + my.i] = lse;
             else
@@ -410,6 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    // Neither CTA of a pair leaves while its partner may still multicast into it
+    // or arrive on its barriers.
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -417,31 +467,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD, class Seqs>
+template <int HD, class Seqs, bool PAIR>
 cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
                        const CUtensorMap& tmV, const Seqs& seqs, cudaStream_t stream) {
     using C = PrefillCfg<HD>;
-    auto kern = fwd_prefill_kernel<HD, Seqs>;
+    auto kern = fwd_prefill_kernel<HD, Seqs, PAIR>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmK, tmV,
-                      seqs);
+                      seqs, PAIR ? 2 : 1);
+}
+
+// Two query heads of one KV head with one split each see the same blocks:
+// launch them as a 2-CTA cluster sharing the K/V loads.
+inline bool use_pairs(const Plan& plan) {
+    return plan.d == 128 && !plan.pack_gqa && plan.G % 2 == 0 && plan.num_splits == 1 && plan.grid_y % 2 == 0;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, cudaStream_t stream) {
+    const bool pair = use_pairs(plan);
     if (!plan.varlen) {
         UniformSeqs u{plan.kv_len[0], plan.splits_b[0]};
-        return plan.d == 128 ? launch_one<128>(plan, p, tmK, tmV, u, stream)
-                             : launch_one<64>(plan, p, tmK, tmV, u, stream);
+        if (plan.d == 128)
+            return pair ? launch_one<128, UniformSeqs, true>(plan, p, tmK, tmV, u, stream)
+                        : launch_one<128, UniformSeqs, false>(plan, p, tmK, tmV, u, stream);
+        return launch_one<64, UniformSeqs, false>(plan, p, tmK, tmV, u, stream);
     }
     VarlenSeqs v;
     fill_varlen(plan, &v);
-    return plan.d == 128 ? launch_one<128>(plan, p, tmK, tmV, v, stream)
-                         : launch_one<64>(plan, p, tmK, tmV, v, stream);
+    if (plan.d == 128)
+        return pair ? launch_one<128, VarlenSeqs, true>(plan, p, tmK, tmV, v, stream)
+                    : launch_one<128, VarlenSeqs, false>(plan, p, tmK, tmV, v, stream);
+    return launch_one<64, VarlenSeqs, false>(plan, p, tmK, tmV, v, stream);
 }
 
 }  // namespace sk

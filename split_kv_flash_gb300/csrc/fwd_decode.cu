@@ -199,6 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc_bf16(128, NP, false, false);
             constexpr uint32_t idesc_pv = make_idesc_bf16(128, NP, true, false);
+            // Descriptors built once; per MMA only a constant is added to the
+            // start-address field (operands lie below 256 KB: no carry).
+            const uint64_t kdesc0 = make_sdesc_sw128(stage_k(0), 16, 1024);
+            const uint64_t vdesc0 = make_sdesc_sw128(stage_v(0), 16384, 1024);
+            const uint64_t qdesc0 = make_sdesc_sw128(sQ, 16, 1024);
+            const uint64_t pdesc0 = make_sdesc_sw128(sP, 16, 1024);
             bool ok = true;
             if (p.inject_stall)
                 ok = mbar_wait(bar_never, 0, wc, (kKernDecode << 8) | kSiteInjected);
@@ -213,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (good) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = make_sdesc_sw128(stage_v(s) + kk * 2048, 16384, 1024);
-                        const uint64_t bd = make_sdesc_sw128(sP + (jj & 1) * C::kPBuf + (kk >> 2) * (NP * 128) +
-                                                                 (kk & 3) * 32, 16, 1024);
+                        const uint64_t a = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
+                        const uint64_t bd =
+                            pdesc0 + uint64_t(((jj & 1) * C::kPBuf + (kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
                         umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_odone(jj & 1));
@@ -232,8 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (good && ok) {
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint64_t a = make_sdesc_sw128(stage_k(s) + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw128(sQ + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t a =
+                            kdesc0 + uint64_t((s * C::kKBytes + (kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                        const uint64_t bd = qdesc0 + uint64_t(((kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
                         umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(bar_sfull(j & 1));

@@ -203,6 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_pv = make_idesc_bf16(128, HD, false, true);
+            // Descriptors are built once; per MMA only a constant is added to the
+            // start-address field (all operands lie below 256 KB, so the field
+            // never carries).  This keeps the single issuing thread ahead of the
+            // tensor pipe.
+            const uint64_t qdesc0 = make_sdesc_sw128(sQ, 16, 1024);
+            const uint64_t kdesc0 = make_sdesc_sw128(stage_k(0), 16, 1024);
+            const uint64_t vdesc0 = make_sdesc_sw128(stage_v(0), 16384, 1024);
             bool ok = true;
             if (p.inject_stall) ok = mbar_wait(bar_never, 0, wc, (kKernPrefill << 8) | kSiteInjected);
             if (nblocks > 0) ok = mbar_wait(bar_qfull, 0, wc, (kKernPrefill << 8) | kSiteMmaQ) && ok;
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         // A = P from TMEM: 16 keys = 8 packed columns per MMA.
-                        const uint64_t bd = make_sdesc_sw128(stage_v(s) + kk * 2048, 16384, 1024);
+                        const uint64_t bd = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
                         umma_bf16_ts(tO, tP0 + (jj & 1) * 64 + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_odone(jj & 1));
@@ -235,8 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (good && ok) {
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint64_t a = make_sdesc_sw128(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw128(stage_k(s) + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint32_t off = uint32_t((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        const uint64_t a = qdesc0 + off;
+                        const uint64_t bd = kdesc0 + uint64_t((s * C::kKBytes) >> 4) + off;
                         umma_bf16(tS0 + (j & 1) * 128, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(bar_sfull(j & 1));

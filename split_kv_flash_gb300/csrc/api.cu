@@ -43,14 +43,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K or V as a 2-D bf16 tensor [rows][Hkv * d]; boxes of 128 rows x 64 columns
-// (128 bytes, the swizzle width), 128-byte swizzle, zero fill past the end.
-bool make_kv_map(CUtensorMap* m, const void* base, int Hkv, int d, long long rows) {
+// K or V as a 2-D bf16 tensor [rows][Hkv * d]; boxes of box_rows rows x 64
+// columns (128 bytes, the swizzle width), 128-byte swizzle, zero fill past the end.
+bool make_kv_map(CUtensorMap* m, const void* base, int Hkv, int d, long long rows, int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cuuint64_t(Hkv) * cuuint64_t(d), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(Hkv) * cuuint64_t(d) * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -187,7 +187,8 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     const void* kb = total_kv > 0 ? k : out;
     const void* vb = total_kv > 0 ? v : out;
     const long long rows = total_kv > 0 ? total_kv : 1;
-    if (!make_kv_map(&tmK, kb, Hkv, d, rows) || !make_kv_map(&tmV, vb, Hkv, d, rows))
+    const int box_rows = kv_box_rows(p);
+    if (!make_kv_map(&tmK, kb, Hkv, d, rows, box_rows) || !make_kv_map(&tmV, vb, Hkv, d, rows, box_rows))
         return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -92,6 +92,10 @@ cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t st
 
 void fill_varlen(const Plan& plan, VarlenSeqs* v);
 
+// Rows per TMA box of the K/V tensor maps: 128 divided by the number of CTAs
+// of a cluster that share (multicast) each K/V block.
+int kv_box_rows(const Plan& plan);
+
 // Launch a partial kernel as a programmatic dependent of the previous work on
 // the stream: it may be scheduled while that work drains and waits for it
 // (griddepcontrol.wait) before touching global memory.

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
             const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
             const int kvh = p.pack_gqa ? ht : ht / p.G;
-            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, 0, l2_policy_evict_first(), wc,
+            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, false, 0u, l2_policy_evict_first(), wc,
                            (kKernDecode << 8) | kSiteProducerEmpty);
         }
     } else if (warp == 1) {

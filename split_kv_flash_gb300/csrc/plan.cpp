@@ -164,7 +164,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     if (path == SK_PATH_DECODE) {
         p.kBlockM = std::max(16, (p.rows + 15) / 16 * 16);
     } else {
-        p.kBlockM = 128;
+        // Prefill kernel: 256-row tiles, two 128-row halves that share each K/V block.
+        p.kBlockM = 256;
     }
     p.num_m_blocks = p.rows == 0 ? 0 : ceil_div_c(p.rows, p.kBlockM);
     p.nblk_max = ceil_div_c(p.max_kv, p.kBlockN);

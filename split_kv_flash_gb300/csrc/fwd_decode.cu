@@ -196,63 +196,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ===================== MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = make_idesc_bf16(128, NP, false, false);
-            constexpr uint32_t idesc_pv = make_idesc_bf16(128, NP, true, false);
-            // Descriptors built once; per MMA only a constant is added to the
-            // start-address field (operands lie below 256 KB: no carry).
-            const uint64_t kdesc0 = make_sdesc_sw128(stage_k(0), 16, 1024);
-            const uint64_t vdesc0 = make_sdesc_sw128(stage_v(0), 16384, 1024);
-            const uint64_t qdesc0 = make_sdesc_sw128(sQ, 16, 1024);
-            const uint64_t pdesc0 = make_sdesc_sw128(sP, 16, 1024);
-            bool ok = true;
-            if (p.inject_stall)
-                ok = mbar_wait(bar_never, 0, wc, (kKernDecode << 8) | kSiteInjected);
-            if (nblocks > 0)
-                ok = mbar_wait(bar_qfull, 0, wc, (kKernDecode << 8) | kSiteMmaQ) && ok;
-            auto issue_pv = [&](int jj) {
-                bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
-                tc_fence_after();
-                const int s = jj % ST;
-                good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull) && good;
-                tc_fence_after();
-                if (good) {
+        // The whole warp runs the schedule (warp-uniform control flow and
+        // descriptors); one elected lane issues every tcgen05 op, so its
+        // commits track exactly the MMAs it issued.
+        const bool leader = elect_one();
+        constexpr uint32_t idesc_qk = make_idesc_bf16(128, NP, false, false);
+        constexpr uint32_t idesc_pv = make_idesc_bf16(128, NP, true, false);
+        // Descriptors built once; per MMA only a constant is added to the
+        // start-address field (operands lie below 256 KB: no carry).
+        const uint64_t kdesc0 = make_sdesc_sw128(stage_k(0), 16, 1024);
+        const uint64_t vdesc0 = make_sdesc_sw128(stage_v(0), 16384, 1024);
+        const uint64_t qdesc0 = make_sdesc_sw128(sQ, 16, 1024);
+        const uint64_t pdesc0 = make_sdesc_sw128(sP, 16, 1024);
+        bool ok = true;
+        if (p.inject_stall)
+            ok = mbar_wait(bar_never, 0, wc, (kKernDecode << 8) | kSiteInjected);
+        if (nblocks > 0)
+            ok = mbar_wait(bar_qfull, 0, wc, (kKernDecode << 8) | kSiteMmaQ) && ok;
+        auto issue_pv = [&](int jj) {
+            bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
+            const int s = jj % ST;
+            good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull) && good;
+            tc_fence_after();
+            __syncwarp();
+            if (leader && good) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
-                        const uint64_t bd =
-                            pdesc0 + uint64_t(((jj & 1) * C::kPBuf + (kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
-                        umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bar_odone(jj & 1));
-                    umma_commit(bar_vempty(s));
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t a = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
+                    const uint64_t bd =
+                        pdesc0 + uint64_t(((jj & 1) * C::kPBuf + (kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
+                    umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
-            };
-            for (int j = 0; j < nblocks; ++j) {
-                const int s = j % ST;
-                bool good = mbar_wait(bar_kfull(s), (j / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
-                if (j >= 2)
-                    good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
-                                     (kKernDecode << 8) | kSiteMmaSEmpty) && good;
-                tc_fence_after();
-                if (good && ok) {
-#pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint64_t a =
-                            kdesc0 + uint64_t((s * C::kKBytes + (kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                        const uint64_t bd = qdesc0 + uint64_t(((kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
-                        umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(bar_sfull(j & 1));
-                    umma_commit(bar_kempty(s));
-                }
-                if (j >= 1) issue_pv(j - 1);
+                umma_commit(bar_odone(jj & 1));
+                umma_commit(bar_vempty(s));
             }
-            if (nblocks >= 1) issue_pv(nblocks - 1);
-            // Every issued MMA completes before TMEM is released.
-            umma_commit(bar_drain);
-            mbar_drain(bar_drain, 0, p.timeout_ns);
+        };
+        for (int j = 0; j < nblocks; ++j) {
+            const int s = j % ST;
+            bool good = mbar_wait(bar_kfull(s), (j / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
+            if (j >= 2)
+                good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
+                                 (kKernDecode << 8) | kSiteMmaSEmpty) && good;
+            tc_fence_after();
+            __syncwarp();
+            if (leader && good && ok) {
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint64_t a =
+                        kdesc0 + uint64_t((s * C::kKBytes + (kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = qdesc0 + uint64_t(((kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
+                    umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(bar_sfull(j & 1));
+                umma_commit(bar_kempty(s));
+            }
+            if (j >= 1) issue_pv(j - 1);
         }
+        if (nblocks >= 1) issue_pv(nblocks - 1);
+        // Every issued MMA completes before TMEM is released.
+        __syncwarp();
+        if (leader) umma_commit(bar_drain);
+        mbar_drain(bar_drain, 0, p.timeout_ns);
     } else {
         // ===================== softmax / correction / epilogue (128 threads)
         const int sidx = threadIdx.x - 64;            // 0..127 for cooperative loops

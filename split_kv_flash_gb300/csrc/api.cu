@@ -43,16 +43,33 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K or V as a 2-D bf16 tensor [rows][Hkv * d]; boxes of box_rows rows x 64
-// columns (128 bytes, the swizzle width), 128-byte swizzle, zero fill past the end.
-bool make_kv_map(CUtensorMap* m, const void* base, int Hkv, int d, long long rows, int box_rows) {
+// K or V as a 2-D bf16 tensor [rows][Hkv * d]; boxes of 128 rows x 64 columns
+// (128 bytes, the swizzle width), 128-byte swizzle, zero fill past the end.
+bool make_kv_map(CUtensorMap* m, const void* base, int Hkv, int d, long long rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cuuint64_t(Hkv) * cuuint64_t(d), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(Hkv) * cuuint64_t(d) * 2};
-    cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+    cuuint32_t box[2] = {64, 128};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Q [B * q_len][Hq][d] as a 4-D bf16 tensor (d, gp, Hq / gp, B * q_len): a box
+// of (64, gp, 1, 128 / gp) is 128 rows of 128 bytes in packed-row order
+// (query position major, the gp query heads of a group minor), 128-byte
+// swizzle, zero fill past the end.
+bool make_q_map(CUtensorMap* m, const void* q, long long rows, int Hq, int d, int gp) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(gp), cuuint64_t(Hq / gp), cuuint64_t(rows)};
+    cuuint64_t strides[3] = {cuuint64_t(d) * 2, cuuint64_t(gp) * cuuint64_t(d) * 2, cuuint64_t(Hq) * cuuint64_t(d) * 2};
+    cuuint32_t box[4] = {64, cuuint32_t(gp), 1, cuuint32_t(128 / gp)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -187,9 +204,17 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     const void* kb = total_kv > 0 ? k : out;
     const void* vb = total_kv > 0 ? v : out;
     const long long rows = total_kv > 0 ? total_kv : 1;
-    const int box_rows = kv_box_rows(p);
-    if (!make_kv_map(&tmK, kb, Hkv, d, rows, box_rows) || !make_kv_map(&tmV, vb, Hkv, d, rows, box_rows))
+    if (!make_kv_map(&tmK, kb, Hkv, d, rows) || !make_kv_map(&tmV, vb, Hkv, d, rows))
         return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    // Prefill tiles take Q by TMA when a 128-row half is whole row groups of the
+    // map (128 % gp == 0) and every row index fits the copy's int32 coordinate.
+    CUtensorMap tmQ;
+    memset(&tmQ, 0, sizeof tmQ);
+    const int q_gp = p.pack_gqa ? p.G : 1;
+    const long long q_rows = (long long)B * q_len;
+    const bool q_tma = p.path == SK_PATH_PREFILL && 128 % q_gp == 0 && q_rows < (1LL << 31);
+    if (q_tma && !make_q_map(&tmQ, q, q_rows, Hq, d, q_gp))
+        return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (Q)");
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     FwdParams fp;
@@ -215,13 +240,15 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     fp.echo_plan = o.debug_echo_plan ? 1 : 0;
     fp.inject_stall = o.debug_inject_stall ? 1 : 0;
     fp.timeout_ns = (unsigned long long)(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
+    fp.q_tma = q_tma ? 1 : 0;
+    fp.q_gp = q_gp;
 
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e;
     if (o.event_begin && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_begin), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
     e = (p.path == SK_PATH_DECODE) ? launch_decode(p, fp, tmK, tmV, stream)
-                                   : launch_prefill(p, fp, tmK, tmV, stream);
+                                   : launch_prefill(p, fp, tmK, tmV, tmQ, stream);
     if (e != cudaSuccess) return fail_cuda(e, "partial kernel launch");
     if (o.event_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_end), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");

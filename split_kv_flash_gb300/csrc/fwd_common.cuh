@@ -46,6 +46,8 @@ struct FwdParams {
     int echo_plan;
     int inject_stall;
     unsigned long long timeout_ns;
+    int q_tma;         // prefill: Q halves arrive by TMA through the 4-D Q map
+    int q_gp;          // query heads per row group of that map (G with PackGQA, else 1)
 };
 
 // Per-sequence lengths, offsets and split counts.  Equal lengths need no table.
@@ -87,39 +89,29 @@ __device__ __forceinline__ RowMap map_row(const FwdParams& p, int ht, int r) {
 cudaError_t launch_decode(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, cudaStream_t stream);
 cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, cudaStream_t stream);
+                           const CUtensorMap& tmV, const CUtensorMap& tmQ, cudaStream_t stream);
 cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 
 void fill_varlen(const Plan& plan, VarlenSeqs* v);
 
-// Rows per TMA box of the K/V tensor maps: 128 divided by the number of CTAs
-// of a cluster that share (multicast) each K/V block.
-int kv_box_rows(const Plan& plan);
-
-// Launch a partial kernel as a programmatic dependent of the previous work on
-// the stream: it may be scheduled while that work drains and waits for it
-// (griddepcontrol.wait) before touching global memory.
-template <class Seqs>
-cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream,
-                       const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const Seqs& seqs,
-                       int cluster_y = 1) {
+// Launch a kernel as a programmatic dependent of the previous work on the
+// stream: it may be scheduled while that work drains and waits for it
+// (griddepcontrol.wait) before touching global memory.  `args` are the kernel's
+// parameters in order.
+template <class... A>
+cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream, const A&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = unsigned(cluster_y);
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = cluster_y > 1 ? 2 : 1;
-    void* args[4] = {const_cast<FwdParams*>(&p), const_cast<CUtensorMap*>(&tmK), const_cast<CUtensorMap*>(&tmV),
-                     const_cast<Seqs*>(&seqs)};
-    return cudaLaunchKernelExC(&cfg, kernel, args);
+    cfg.numAttrs = 1;
+    void* ptrs[] = {const_cast<void*>(static_cast<const void*>(&args))...};
+    return cudaLaunchKernelExC(&cfg, kernel, ptrs);
 }
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device).

@@ -186,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
-        // ===================== TMA producer (K and V rings)
-        if (lane == 0) {
-            const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
-            const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
-            const int kvh = p.pack_gqa ? ht : ht / p.G;
-            produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, false, 0u, l2_policy_evict_first(), wc,
-                           (kKernDecode << 8) | kSiteProducerEmpty);
-        }
+        // ===================== TMA producer (K and V rings): the whole warp
+        // runs the loop, one elected lane issues the copies.
+        const bool leader = elect_one();
+        const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
+        const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
+        const int kvh = p.pack_gqa ? ht : ht / p.G;
+        produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, false, l2_policy_evict_first(), wc,
+                       (kKernDecode << 8) | kSiteProducerEmpty, leader);
     } else if (warp == 1) {
         // ===================== MMA issuer
         // The whole warp runs the schedule (warp-uniform control flow and
@@ -209,8 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qdesc0 = make_sdesc_sw128(sQ, 16, 1024);
         const uint64_t pdesc0 = make_sdesc_sw128(sP, 16, 1024);
         bool ok = true;
-        if (p.inject_stall)
-            ok = mbar_wait(bar_never, 0, wc, (kKernDecode << 8) | kSiteInjected);
+        if (p.inject_stall) {
+            // The injected stall gives up first (half the limit), so the status
+            // names it rather than a wait that starves behind it.
+            const WaitCtl wc_half{wc.abort_flag, wc.status, wc.limit_ns / 2};
+            ok = mbar_wait(bar_never, 0, wc_half, (kKernDecode << 8) | kSiteInjected);
+        }
         if (nblocks > 0)
             ok = mbar_wait(bar_qfull, 0, wc, (kKernDecode << 8) | kSiteMmaQ) && ok;
         auto issue_pv = [&](int jj) {

@@ -20,16 +20,14 @@
 // shorter (the upper rows of a causal tile see one block less) skips the steps
 // outside it.
 //
-// Query heads that share a KV head and see the same blocks (no PackGQA, one
-// split) can run as clusters of CL = 2 or 4 CTAs: each CTA loads 128 / CL rows
-// of every K/V block and multicasts them to the whole cluster, which divides
-// the L2 -> SM traffic of the K/V stream by CL.  Measured on GB300 at 8192
-// tokens the lock-step of a cluster costs more than the L2 traffic it saves,
-// so the default build keeps CL = 1 (SK_PREFILL_MAX_CLUSTER raises it).
+// Q halves arrive by TMA (a 4-D map whose 128-row box is in packed-row order)
+// unless a half is not whole row groups of that map; then the softmax warps
+// load them.
 //
-// Warp roles (320 threads): warp 0 TMA producer (K/V rings), warp 1 TMEM owner
-// and MMA issuer, warps 2-5 softmax + correction + epilogue of half 0, warps
-// 6-9 the same for half 1.
+// Warp roles (320 threads): warp 0 TMA producer (Q, K/V rings), warp 1 TMEM
+// owner and MMA issuer (both run whole, warp-uniform; one elected lane issues
+// the copies / MMAs), warps 2-5 softmax + correction + epilogue of half 0,
+// warps 6-9 the same for half 1.
 #include <math.h>
 
 #include "fwd_common.cuh"
@@ -77,10 +75,11 @@ struct PrefillCfg {
     static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
 
-template <int HD, class Seqs, int CL>
+template <int HD, class Seqs>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_prefill_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Seqs seqs) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ Seqs seqs) {
     using C = PrefillCfg<HD>;
     constexpr int KST = C::kStagesK;
     constexpr int VST = C::kStagesV;
@@ -154,14 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < KST; ++s) {
             mbar_init(bar_kfull(s), 1);
-            mbar_init(bar_kempty(s), CL);  // released by every CTA of the cluster
+            mbar_init(bar_kempty(s), 1);
         }
         for (int s = 0; s < VST; ++s) {
             mbar_init(bar_vfull(s), 1);
-            mbar_init(bar_vempty(s), CL);
+            mbar_init(bar_vempty(s), 1);
         }
         for (int t = 0; t < kHalves; ++t) {
-            mbar_init(bar_qfull(t), 128);
+            mbar_init(bar_qfull(t), p.q_tma ? 1 : 128);  // TMA transaction, or every thread of the half
             mbar_init(bar_sfull(t), 1);
             mbar_init(bar_pfull(t), 4);  // one arrival per softmax warp
             mbar_init(bar_ofinal(t), 1);
@@ -178,10 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if (p.q_tma) tma_prefetch_desc(&tmQ);
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CL > 1) cluster_sync();  // the peers' barriers are initialised before any multicast
     tc_fence_after();
     // Everything above touched only shared memory, TMEM and kernel parameters.
     // Under programmatic dependent launch this grid may start while the previous
@@ -195,14 +194,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
-        if (lane == 0) {
-            // K/V of one head are re-read by the other m blocks: keep them in L2.
-            const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
-            const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
-            produce_kv<HD, CL>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, true,
-                               CL > 1 ? cluster_ctarank() : 0u, l2_policy_evict_last(), wc,
-                               (kKernPrefill << 8) | kSiteProducerEmpty);
+        // ===================== producer: Q halves, then the K/V rings
+        const bool leader = elect_one();
+        if (p.q_tma && leader) {
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) {
+                mbar_arrive_expect_tx(bar_qfull(t), C::kQBytes);
+                const int qrow = b * p.sq + (m0 + 128 * t) / p.q_gp;
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c)
+                    tma_load_4d(sQ + uint32_t(t * C::kQBytes + c * 16384), &tmQ, bar_qfull(t), c * 64, 0, ht, qrow,
+                                l2_policy_evict_first());
+            }
         }
+        __syncwarp();
+        // K/V of one head are re-read by the other m blocks: keep them in L2.
+        const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
+        const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
+        produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, true, l2_policy_evict_last(),
+                       wc, (kKernPrefill << 8) | kSiteProducerEmpty, leader);
+        // Q copies land before the CTA exits (the MMA waited for them unless it gave up).
+        if (p.q_tma)
+            for (int t = 0; t < kHalves; ++t) mbar_drain(bar_qfull(t), 0, wc.limit_ns);
     } else if (warp == 1) {
         // The whole warp runs the MMA schedule (warp-uniform control flow, so
         // descriptors and loop state stay warp-uniform); one elected lane issues
@@ -217,14 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t kdesc0 = make_sdesc_sw128(stage_k(0), 16, 1024);
         const uint64_t vdesc0 = make_sdesc_sw128(stage_v(0), 16384, 1024);
         bool ok = true;
-        if (p.inject_stall) ok = mbar_wait(bar_never, 0, wc, (kKernPrefill << 8) | kSiteInjected);
-        // A ring slot is free once every CTA of the cluster has consumed it.
-        auto release = [&](uint32_t bar) {
-            if constexpr (CL > 1)
-                umma_commit_mc(bar, uint16_t((1u << CL) - 1u));
-            else
-                umma_commit(bar);
-        };
+        if (p.inject_stall) {
+            // The injected stall gives up first (half the limit), so the status
+            // names it rather than a wait that starves behind it.
+            const WaitCtl wc_half{wc.abort_flag, wc.status, wc.limit_ns / 2};
+            ok = mbar_wait(bar_never, 0, wc_half, (kKernPrefill << 8) | kSiteInjected);
+        }
         auto active = [&](int t, int j) { return j >= first[t] && j < first[t] + count[t]; };
         // O_t += P_t . V(j), the i-th block of half t.  P_t sits in the upper
         // columns of S_t; the QK^T that next overwrites S_t is issued after
@@ -262,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_wait(bar_vfull((j - 1) % VST), ((j - 1) / VST) & 1, wc,
                                   (kKernPrefill << 8) | kSiteMmaFull);
                     __syncwarp();
-                    if (leader) release(bar_vempty((j - 1) % VST));
+                    if (leader) umma_commit(bar_vempty((j - 1) % VST));
                 }
                 if (j < nblocks && active(t, j)) {
                     const int s = j % KST;
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j < nblocks) {
                 if (!k_ready) mbar_wait(bar_kfull(j % KST), (j / KST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull);
                 __syncwarp();
-                if (leader) release(bar_kempty(j % KST));
+                if (leader) umma_commit(bar_kempty(j % KST));
             }
         }
         __syncwarp();
@@ -311,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hi_t = br.hi - first[t];                  // half's blocks: hi_t - 1 down to hi_t - cnt
         const uint32_t sQt = sQ + uint32_t(t * C::kQBytes);
 
-        // Q half -> smem, K-major 128B swizzle (granule g of row rr at sw128_offset).
-        // All of a thread's loads are issued before any store so that they overlap.
-        {
+        // Q half -> smem when it does not come by TMA: K-major 128B swizzle
+        // (granule g of row rr at sw128_offset); loads are issued before any store.
+        if (!p.q_tma) {
             constexpr int kGran = HD / 8;
             uint4 val[kGran];
 #pragma unroll
@@ -339,8 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : "memory");
             }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(bar_qfull(t));
+        if (!p.q_tma) {
+            fence_proxy_async_smem();
+            mbar_arrive(bar_qfull(t));
+        }
 
         const bool row_ok = r < rows_valid;
         const RowMap my = map_row(p, ht, mt + (row_ok ? r : 0));
@@ -484,9 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
-    // No CTA of a cluster leaves while a peer may still multicast into it or
-    // arrive on its barriers.
-    if constexpr (CL > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -494,58 +504,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD, class Seqs, int CL>
-cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
-                       const CUtensorMap& tmV, const Seqs& seqs, cudaStream_t stream) {
+template <int HD, class Seqs>
+cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmQ, const Seqs& seqs, cudaStream_t stream) {
     using C = PrefillCfg<HD>;
-    auto kern = fwd_prefill_kernel<HD, Seqs, CL>;
+    auto kern = fwd_prefill_kernel<HD, Seqs>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmK, tmV,
-                      seqs, CL);
-}
-
-#ifndef SK_PREFILL_MAX_CLUSTER
-#define SK_PREFILL_MAX_CLUSTER 1
-#endif
-
-// CTAs per cluster: consecutive grid-y indices are query heads h, h + 1, ... of
-// one KV head when nothing is packed and there is one split, so clusters of
-// CL | G CTAs see identical block ranges.
-int prefill_cluster(const Plan& plan) {
-    if (plan.pack_gqa || plan.num_splits != 1) return 1;
-    if (SK_PREFILL_MAX_CLUSTER >= 4 && plan.G % 4 == 0) return 4;
-    if (SK_PREFILL_MAX_CLUSTER >= 2 && plan.G % 2 == 0) return 2;
-    return 1;
-}
-
-template <int HD, class Seqs>
-cudaError_t launch_hd(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                      const Seqs& seqs, cudaStream_t stream) {
-    switch (prefill_cluster(plan)) {
-        case 4: return launch_one<HD, Seqs, 4>(plan, p, tmK, tmV, seqs, stream);
-        case 2: return launch_one<HD, Seqs, 2>(plan, p, tmK, tmV, seqs, stream);
-        default: return launch_one<HD, Seqs, 1>(plan, p, tmK, tmV, seqs, stream);
-    }
+                      tmQ, seqs);
 }
 
 }  // namespace
 
-int kv_box_rows(const Plan& plan) { return plan.path == SK_PATH_PREFILL ? 128 / prefill_cluster(plan) : 128; }
-
-cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, cudaStream_t stream) {
+cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const CUtensorMap& tmQ, cudaStream_t stream) {
     if (plan.kBlockM != 128 * kHalves || plan.kBlockN != 128) return cudaErrorInvalidValue;
     if (!plan.varlen) {
         UniformSeqs u{plan.kv_len[0], plan.splits_b[0]};
-        if (plan.d == 128) return launch_hd<128, UniformSeqs>(plan, p, tmK, tmV, u, stream);
-        return launch_hd<64, UniformSeqs>(plan, p, tmK, tmV, u, stream);
+        if (plan.d == 128) return launch_one<128, UniformSeqs>(plan, p, tmK, tmV, tmQ, u, stream);
+        return launch_one<64, UniformSeqs>(plan, p, tmK, tmV, tmQ, u, stream);
     }
     VarlenSeqs v;
     fill_varlen(plan, &v);
-    if (plan.d == 128) return launch_hd<128, VarlenSeqs>(plan, p, tmK, tmV, v, stream);
-    return launch_hd<64, VarlenSeqs>(plan, p, tmK, tmV, v, stream);
+    if (plan.d == 128) return launch_one<128, VarlenSeqs>(plan, p, tmK, tmV, tmQ, v, stream);
+    return launch_one<64, VarlenSeqs>(plan, p, tmK, tmV, tmQ, v, stream);
 }
 
 }  // namespace sk

@@ -6,6 +6,10 @@
 // so the slots free up in the order K(j), V(j-1), K(j+1), V(j), ...; the
 // producer waits for them in exactly that order (bounded waits that suspend the
 // thread).
+//
+// The whole producer warp runs these loops (warp-uniform control flow); one
+// elected lane, `leader`, issues the copies.  A ring position counts blocks
+// across the tiles a persistent CTA visits: slot pos % slots, use pos / slots.
 #pragma once
 #include "sm103_ptx.cuh"
 
@@ -24,62 +28,63 @@ struct KvRing {
     int slots;
 };
 
-// One block into ring slot j % slots.  With CL > 1 the CTA is rank `rank` of a
-// cluster of CL CTAs that visit the same blocks: it loads rows
-// [rank * 128 / CL, (rank + 1) * 128 / CL) of the block and multicasts them to
-// every CTA of the cluster, so each block leaves L2 once per cluster.  Every
-// CTA's full barrier expects the whole block (its own rows and the peers');
-// every empty barrier counts one release from each CTA of the cluster.
-template <int HD, int CL>
-__device__ __forceinline__ bool load_block(const CUtensorMap* tm, const KvRing& R, int j, int x0, int y0,
-                                           int nblocks, bool desc, uint32_t rank, uint64_t policy,
-                                           const WaitCtl& wc, int where) {
+// One 128-row block (rows y .. y + 127, columns x0 .. x0 + HD) into ring position pos.
+template <int HD>
+__device__ __forceinline__ bool load_block(const CUtensorMap* tm, const KvRing& R, int pos, int x0, int y,
+                                           uint64_t policy, const WaitCtl& wc, int where, bool leader) {
     constexpr uint32_t kBytes = 128u * HD * 2u;
-    constexpr int kRows = 128 / CL;  // rows per TMA box
-    const int s = j % R.slots, u = j / R.slots;
-    if (u >= 1 && !mbar_wait(R.empty + 8u * s, (u - 1) & 1, wc, where)) return false;
-    mbar_arrive_expect_tx(R.full + 8u * s, kBytes);
-    const int y = y0 + visit_block(j, nblocks, desc) * 128 + int(rank) * kRows;
+    const int s = pos % R.slots, u = pos / R.slots;
+    const bool ok = __all_sync(0xffffffffu, u < 1 || mbar_wait(R.empty + 8u * s, (u - 1) & 1, wc, where));
+    if (!ok) return false;
+    if (leader) {
+        mbar_arrive_expect_tx(R.full + 8u * s, kBytes);
 #pragma unroll
-    for (int c = 0; c < HD / 64; ++c) {
-        const uint32_t dst = R.base + s * R.stride + c * 16384 + rank * uint32_t(kRows * 128);
-        if constexpr (CL == 1)
-            tma_load_2d(dst, tm, R.full + 8u * s, x0 + c * 64, y, policy);
-        else
-            tma_load_2d_mc(dst, tm, R.full + 8u * s, x0 + c * 64, y, uint16_t((1u << CL) - 1u), policy);
+        for (int c = 0; c < HD / 64; ++c)
+            tma_load_2d(R.base + s * R.stride + c * 16384, tm, R.full + 8u * s, x0 + c * 64, y, policy);
     }
     return true;
 }
 
-// Loads K and V blocks of rows y0 + 128 * visit_block(j), j in [0, nblocks),
-// columns x0 .. x0 + HD (HD / 64 boxes of 64 columns, 16 KB apart in a slot).
-template <int HD, int CL = 1>
+// K and V blocks of rows y0 + 128 * visit_block(j), j in [0, nblocks), into
+// ring positions g0 + j.  kpos / vpos advance past every load issued, so the
+// caller can drain exactly those; returns false once a wait has given up.
+template <int HD>
+__device__ __forceinline__ bool produce_kv_tile(const CUtensorMap* tmK, const CUtensorMap* tmV, const KvRing& K,
+                                                const KvRing& V, int g0, int nblocks, int x0, int y0, bool desc,
+                                                uint64_t policy, const WaitCtl& wc, int where, bool leader,
+                                                int& kpos, int& vpos) {
+    auto row = [&](int j) { return y0 + visit_block(j, nblocks, desc) * 128; };
+    if (nblocks > 0) {
+        if (!load_block<HD>(tmK, K, g0, x0, row(0), policy, wc, where, leader)) return false;
+        kpos = g0 + 1;
+    }
+    for (int j = 1; j <= nblocks; ++j) {
+        if (j < nblocks) {
+            if (!load_block<HD>(tmK, K, g0 + j, x0, row(j), policy, wc, where, leader)) return false;
+            kpos = g0 + j + 1;
+        }
+        if (!load_block<HD>(tmV, V, g0 + j - 1, x0, row(j - 1), policy, wc, where, leader)) return false;
+        vpos = g0 + j;
+    }
+    return true;
+}
+
+// Before the CTA exits: the last load of every slot (ring positions below
+// `loaded`) must have landed.
+__device__ __forceinline__ void drain_ring(const KvRing& R, int loaded, uint64_t limit_ns) {
+    for (int pos = loaded - 1; pos >= 0 && pos >= loaded - R.slots; --pos)
+        mbar_drain(R.full + 8u * (pos % R.slots), (pos / R.slots) & 1, limit_ns);
+}
+
+// Single-tile form: stream one range, then drain what was issued.
+template <int HD>
 __device__ __forceinline__ void produce_kv(const CUtensorMap* tmK, const CUtensorMap* tmV, const KvRing& K,
                                            const KvRing& V, int nblocks, int x0, int y0, bool desc,
-                                           uint32_t rank, uint64_t policy, const WaitCtl& wc, int where) {
-    int jk = 0, jv = 0;  // blocks issued on each ring
-    if (nblocks > 0 && load_block<HD, CL>(tmK, K, 0, x0, y0, nblocks, desc, rank, policy, wc, where)) jk = 1;
-    for (int j = 1; j <= nblocks && jk == j; ++j) {
-        if (j < nblocks) {
-            if (!load_block<HD, CL>(tmK, K, j, x0, y0, nblocks, desc, rank, policy, wc, where)) break;
-            jk = j + 1;
-        }
-        if (!load_block<HD, CL>(tmV, V, j - 1, x0, y0, nblocks, desc, rank, policy, wc, where)) break;
-        jv = j;
-    }
-    // Drain: the last load of every slot must land before the CTA exits.
-    for (int j = jk - 1; j >= 0 && j >= jk - K.slots; --j)
-        mbar_drain(K.full + 8u * (j % K.slots), (j / K.slots) & 1, wc.limit_ns);
-    for (int j = jv - 1; j >= 0 && j >= jv - V.slots; --j)
-        mbar_drain(V.full + 8u * (j % V.slots), (j / V.slots) & 1, wc.limit_ns);
-    if constexpr (CL > 1) {
-        // The peers' MMAs release this CTA's slots remotely: wait for the last
-        // release of every slot, so none arrives after the CTA has left.
-        for (int j = nblocks - 1; j >= 0 && j >= nblocks - K.slots; --j)
-            mbar_drain(K.empty + 8u * (j % K.slots), (j / K.slots) & 1, wc.limit_ns);
-        for (int j = nblocks - 1; j >= 0 && j >= nblocks - V.slots; --j)
-            mbar_drain(V.empty + 8u * (j % V.slots), (j / V.slots) & 1, wc.limit_ns);
-    }
+                                           uint64_t policy, const WaitCtl& wc, int where, bool leader) {
+    int kpos = 0, vpos = 0;
+    produce_kv_tile<HD>(tmK, tmV, K, V, 0, nblocks, x0, y0, desc, policy, wc, where, leader, kpos, vpos);
+    drain_ring(K, kpos, wc.limit_ns);
+    drain_ring(V, vpos, wc.limit_ns);
 }
 
 }  // namespace sk

@@ -160,9 +160,11 @@ def file_sha(paths):
 
 
 DECODE_SOURCES = ["split_kv_flash_gb300/csrc/fwd_decode.cu", "split_kv_flash_gb300/csrc/sm103_ptx.cuh",
-                  "split_kv_flash_gb300/csrc/fwd_common.cuh", "split_kv_flash_gb300/csrc/block_range.h"]
+                  "split_kv_flash_gb300/csrc/fwd_common.cuh", "split_kv_flash_gb300/csrc/block_range.h",
+                  "split_kv_flash_gb300/csrc/kv_producer.cuh"]
 PREFILL_SOURCES = ["split_kv_flash_gb300/csrc/fwd_prefill.cu", "split_kv_flash_gb300/csrc/sm103_ptx.cuh",
-                   "split_kv_flash_gb300/csrc/fwd_common.cuh", "split_kv_flash_gb300/csrc/block_range.h"]
+                   "split_kv_flash_gb300/csrc/fwd_common.cuh", "split_kv_flash_gb300/csrc/block_range.h",
+                   "split_kv_flash_gb300/csrc/kv_producer.cuh"]
 
 
 def ncu_traffic(kernel_key, sources):

@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep")
     return ap.parse_args()
 
 
@@ -339,6 +340,64 @@ def gpu_prefill(sk, w, steps, warmup, device):
     return statistics.median(ms), info
 
 
+def sweep_workloads():
+    """The other configurations, one representative set each (tiny decode, the
+    other GQA decode lengths, speculative verify, varlen decode)."""
+    ws = [wl.tiny_decode()]
+    ws += [wl.gqa_decode(kv) for kv in (4096, 16384, 32768)]
+    ws += [wl.spec_verify(q, 8192) for q in (9, 17, 33)] + [wl.spec_verify(17, 2048)]
+    ws += [wl.varlen_decode(b) for b in (1, 8, 32)]
+    return ws
+
+
+def gpu_sweep(sk, device, hbm_peak, reps=20, warmup=3):
+    """Whole-call time (partial + combine, CUDA events on the stream around the
+    call) per configuration, L2 flushed before every timed call.  Inputs are
+    drawn on the device (throughput does not depend on the values; parity is
+    tested on the seeded CPU draws)."""
+    rows = []
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for w in sweep_workloads():
+        g = torch.Generator(device=device).manual_seed(w.seed)
+        q = torch.randn((w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
+        k = (torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g) * w.k_scale).to(torch.bfloat16)
+        v = torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g).to(torch.bfloat16)
+        out = torch.empty((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
+        info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left)
+        wsb = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
+
+        def call():
+            sk.sk_attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.scale,
+                           w.causal, w.window_left, wsb, wsb.numel(), stream)
+
+        for _ in range(warmup):
+            call()
+        evb = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        eve = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        for i in range(reps):
+            flush.fill_(float(i))
+            evb[i].record(stream)
+            call()
+            eve[i].record(stream)
+        torch.cuda.synchronize(device)
+        st, where = sk.sk_attn_workspace_status(wsb)
+        if st != 0:
+            raise RuntimeError("device status %d at %d (%s)" % (st, where, w.name))
+        ms = statistics.median(evb[i].elapsed_time(eve[i]) for i in range(reps))
+        nbytes = decode_bytes(w)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        row = {"workload": w.name, "us": ms * 1e3, "bytes": nbytes, "gbs": gbs,
+               "frac_of_hbm_peak": gbs / hbm_peak, "path": "decode" if info.path == 1 else "prefill",
+               "splits": info.num_splits, "ctas": info.num_ctas}
+        if w.q_len > 1:
+            row["tflops"] = prefill_flops(w) / (ms * 1e-3) / 1e12
+        rows.append(row)
+        del q, k, v, out, lse, wsb
+    return rows
+
+
 _pg = None
 
 
@@ -510,6 +569,12 @@ def main():
             "unit": "TFLOP/s", "peak": bf16_peak, "peak_source": peak_src + " bf16_tflops (burst)",
             "flop_count": "4 * d per visible (query, key) pair per head", **pre,
             "traffic": ncu_traffic("prefill_causal_8192", PREFILL_SOURCES)}
+    if rank == 0 and not args.no_sweep:
+        result["sweep"] = {
+            "unit": "GB/s", "peak": hbm_peak, "bound": "hbm",
+            "method": "median of 20 whole calls (partial + combine), CUDA events on the stream, "
+                      "L2 flushed before each call; bytes = K + V of every sequence + Q + O + LSE",
+            "rows": gpu_sweep(sk, device, hbm_peak)}
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)
     if rank == 0:

@@ -8,13 +8,17 @@
 //   O   = sum_s exp(LSE_s - LSE) * O_s         -> bf16
 // All partials at -inf: O = 0, LSE = -inf.
 //
-// One CTA of 8 warps per output row.  The row's partials are spread over the
-// warps (warp w takes splits w, w + 8, ...), so every load of the row is in
-// flight at once and the merge costs about one L2 round trip; lane c holds the
-// float4 columns c (and c + 32 when d = 256 ...) of the row.  The kernel is
-// launched as a programmatic dependent of the partial kernel: it is scheduled
-// while the partial kernel runs and waits (griddepcontrol.wait) for that
-// grid's completion and memory before it reads anything.
+// Two shapes of the same merge:
+//  - many splits (S > 16; long-context decode: few rows, up to 128 splits):
+//    one CTA of 8 warps per output row.  The row's partials are spread over
+//    the warps (warp w takes splits w, w + 8, ...), so every load of the row is
+//    in flight at once and the merge costs about one L2 round trip;
+//  - few splits (S <= 16; verify, batched decode: many rows, few splits): one
+//    warp per row, 8 rows per CTA, lane s holding split s's LSE and lane c the
+//    float4 columns c of the row, so a CTA is not launched for a few loads.
+// Both are launched as programmatic dependents of the partial kernel: they are
+// scheduled while the partial kernel runs and wait (griddepcontrol.wait) for
+// that grid's completion and memory before they read anything.
 #include <math.h>
 
 #include "fwd_common.cuh"
@@ -117,13 +121,70 @@ __global__ void __launch_bounds__(32 * kWarps)
     }
 }
 
+constexpr int kRowsMaxSplits = 16;  // the warp-per-row shape handles up to this many splits
+
+template <int HD, class Seqs>
+__global__ void __launch_bounds__(32 * kWarps)
+    combine_rows_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ Seqs seqs, long long rows) {
+    constexpr int kCols4 = HD / 4;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * kWarps + warp;
+    griddep_launch_dependents();  // the next call's partial kernel may start its prologue
+    griddep_wait();
+    if (row >= rows) return;
+    const int b = int(row / ((long long)p.Hq * p.sq));
+    const int rem = int(row - (long long)b * p.Hq * p.sq);
+    const int h = rem / p.sq;
+    const int i = rem - h * p.sq;
+    const int S = seqs.splits_of(b);
+    if (S <= 1) return;  // written directly by the partial kernel
+    const size_t stride = (size_t)p.B * p.Hq * p.sq;  // between splits of one row
+    const size_t base = ((size_t)b * p.Hq + h) * p.sq + i;
+
+    // log-sum-exp over the splits: lane s holds split s
+    const float l = (lane < S) ? __ldcg(p.lse_part + lane * stride + base) : -INFINITY;
+    float mx = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = (l == -INFINITY) ? 0.f : exp2f((l - mx) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float lse = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+    const float w = (l == -INFINITY || lse == -INFINITY) ? 0.f : exp2f((l - lse) * kLog2e);
+
+    // weighted sum of the O partials: lane c holds float4 column c
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(p.o_part + base * HD) + lane;
+    const size_t stride4 = stride * (HD / 4);
+#pragma unroll 4
+    for (int s = 0; s < S; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w, s);
+        if (lane < kCols4) {
+            const float4 v = __ldcg(src + s * stride4);
+            acc.x += ws * v.x;
+            acc.y += ws * v.y;
+            acc.z += ws * v.z;
+            acc.w += ws * v.w;
+        }
+    }
+    if (lane < kCols4) {
+        uint2 packed;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.sq + i) * p.Hq + h) * HD + lane * 4) = packed;
+    }
+    if (lane == 0) p.lse[base] = lse;
+}
+
 template <int HD, class Seqs>
 cudaError_t launch_c(const Plan& plan, const FwdParams& p, const Seqs& seqs, cudaStream_t stream) {
     const long long rows = (long long)plan.B * plan.Hq * plan.sq;
     if (rows <= 0) return cudaSuccess;
     if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(rows));
     cfg.blockDim = dim3(32 * kWarps);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -132,6 +193,11 @@ cudaError_t launch_c(const Plan& plan, const FwdParams& p, const Seqs& seqs, cud
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (plan.num_splits <= kRowsMaxSplits) {
+        cfg.gridDim = dim3(unsigned((rows + kWarps - 1) / kWarps));
+        return cudaLaunchKernelEx(&cfg, combine_rows_kernel<HD, Seqs>, p, seqs, rows);
+    }
+    cfg.gridDim = dim3(unsigned(rows));
     return cudaLaunchKernelEx(&cfg, combine_kernel<HD, Seqs>, p, seqs);
 }
 

@@ -316,6 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l_t[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) l_t[q] = 0.f;
+        // Running row maxima, identical in every thread (the shared copy sm_m is
+        // only read back after a block raised them).
+        float m_reg[NP];
+#pragma unroll
+        for (int q = 0; q < NP; ++q) m_reg[q] = -INFINITY;
+        const float sl2 = p.scale_log2;
+        __nv_bfloat16* const p_smem = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP);
 
         for (int j = 0; j < nblocks; ++j) {
             const int n = br.lo + j;
@@ -334,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    (has_window && blk_first < diag_hi - p.window_left);
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-                float v = x[q] * p.scale_log2;
+                float v = x[q] * sl2;
                 if (q >= rows_valid) v = -INFINITY;
                 if (need_mask) {
                     const int dg = sm_diag[q];
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool need = false;
 #pragma unroll
-            for (int q = 0; q < NP; ++q) need |= x[q] > sm_m[q] + kRescaleThreshold;
+            for (int q = 0; q < NP; ++q) need |= x[q] > m_reg[q] + kRescaleThreshold;
             const bool need_all = named_bar_or(1, 128, need);
             if (need_all) {
 #pragma unroll
@@ -364,11 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_bar_sync(1, 128);
 #pragma unroll
-                for (int q = 0; q < NP; ++q) l_t[q] *= sm_alpha[q];
+                for (int q = 0; q < NP; ++q) {
+                    l_t[q] *= sm_alpha[q];
+                    m_reg[q] = sm_m[q];
+                }
             }
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-                const float mq = sm_m[q];
+                const float mq = m_reg[q];
                 const float pv = (mq == -INFINITY) ? 0.f : fast_exp2(x[q] - mq);
                 l_t[q] += pv;
                 x[q] = pv;
@@ -393,19 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
-            // P^T[q][kt] (bf16) -> smem, K-major over keys, 128B swizzle.
+            // P^T[q][kt] (bf16) -> smem, K-major over keys, 128B swizzle.  Plain
+            // stores, so the compiler may schedule them; the proxy fence below
+            // orders them before the MMA reads the buffer.
             {
-                const uint32_t base = sP + (j & 1) * C::kPBuf + (kt >> 6) * (NP * 128);
+                const uint32_t base = uint32_t((j & 1) * C::kPBuf + (kt >> 6) * (NP * 128));
                 const int g = (kt & 63) >> 3;
                 const uint32_t within = (kt & 7) * 2;
 #pragma unroll
-                for (int q = 0; q < NP; ++q) {
-                    const __nv_bfloat16 hv = __float2bfloat16_rn(x[q]);
-                    const uint16_t bits = *reinterpret_cast<const uint16_t*>(&hv);
-                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(base + sw128_offset(q, g) + within),
-                                 "h"(bits)
-                                 : "memory");
-                }
+                for (int q = 0; q < NP; ++q)
+                    p_smem[(base + sw128_offset(q, g) + within) >> 1] = __float2bfloat16_rn(x[q]);
             }
             fence_proxy_async_smem();
             tc_fence_before();

@@ -339,16 +339,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int blk_first = n * 128, blk_last = n * 128 + 127;
             const bool need_mask = (blk_last >= sk) || (has_causal && blk_last > diag_lo) ||
                                    (has_window && blk_first < diag_hi - p.window_left);
+            // Scale, then the masks as separate warp-uniform passes: padding rows
+            // only when the tile has them, keys only on boundary blocks.
 #pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                float v = x[q] * sl2;
-                if (q >= rows_valid) v = -INFINITY;
-                if (need_mask) {
+            for (int q = 0; q < NP; ++q) x[q] *= sl2;
+            if (rows_valid < NP) {
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    if (q >= rows_valid) x[q] = -INFINITY;
+            }
+            if (need_mask) {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
                     const int dg = sm_diag[q];
                     if (key >= sk || (has_causal && key > dg) || (has_window && key < dg - p.window_left))
-                        v = -INFINITY;
+                        x[q] = -INFINITY;
                 }
-                x[q] = v;
             }
             bool need = false;
 #pragma unroll

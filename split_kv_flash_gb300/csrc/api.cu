@@ -75,6 +75,23 @@ bool make_q_map(CUtensorMap* m, const void* q, long long rows, int Hq, int d, in
     return r == CUDA_SUCCESS;
 }
 
+// O [B][q_len][Hq][d] as a 5-D bf16 tensor (d, gp, Hq / gp, q_len, B): the same
+// packed-row boxes as the Q map, with the sequence as its own dimension so that
+// a store clips the rows past q_len instead of writing into the next sequence.
+bool make_o_map(CUtensorMap* m, void* o, int B, int q_len, int Hq, int d, int gp) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[5] = {cuuint64_t(d), cuuint64_t(gp), cuuint64_t(Hq / gp), cuuint64_t(q_len), cuuint64_t(B)};
+    const cuuint64_t row = cuuint64_t(Hq) * cuuint64_t(d) * 2;
+    cuuint64_t strides[4] = {cuuint64_t(d) * 2, cuuint64_t(gp) * cuuint64_t(d) * 2, row, row * cuuint64_t(q_len)};
+    cuuint32_t box[5] = {64, cuuint32_t(gp), 1, cuuint32_t(128 / gp), 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, o, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
     int sms = 0, major = 0, minor = 0;
 };
@@ -215,6 +232,12 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     const bool q_tma = p.path == SK_PATH_PREFILL && 128 % q_gp == 0 && q_rows < (1LL << 31);
     if (q_tma && !make_q_map(&tmQ, q, q_rows, Hq, d, q_gp))
         return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (Q)");
+    // Final prefill outputs (one split per sequence) leave through the same boxes.
+    CUtensorMap tmO;
+    memset(&tmO, 0, sizeof tmO);
+    const bool o_tma = q_tma && !p.needs_combine;
+    if (o_tma && !make_o_map(&tmO, out, B, q_len, Hq, d, q_gp))
+        return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (O)");
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     FwdParams fp;
@@ -242,13 +265,14 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     fp.timeout_ns = (unsigned long long)(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
     fp.q_tma = q_tma ? 1 : 0;
     fp.q_gp = q_gp;
+    fp.o_tma = o_tma ? 1 : 0;
 
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e;
     if (o.event_begin && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_begin), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
     e = (p.path == SK_PATH_DECODE) ? launch_decode(p, fp, tmK, tmV, stream)
-                                   : launch_prefill(p, fp, tmK, tmV, tmQ, stream);
+                                   : launch_prefill(p, fp, tmK, tmV, tmQ, tmO, stream);
     if (e != cudaSuccess) return fail_cuda(e, "partial kernel launch");
     if (o.event_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_end), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");

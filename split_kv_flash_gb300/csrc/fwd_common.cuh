@@ -48,6 +48,7 @@ struct FwdParams {
     unsigned long long timeout_ns;
     int q_tma;         // prefill: Q halves arrive by TMA through the 4-D Q map
     int q_gp;          // query heads per row group of that map (G with PackGQA, else 1)
+    int o_tma;         // prefill: final O halves leave by TMA through the 5-D O map
 };
 
 // Per-sequence lengths, offsets and split counts.  Equal lengths need no table.
@@ -89,7 +90,8 @@ __device__ __forceinline__ RowMap map_row(const FwdParams& p, int ht, int r) {
 cudaError_t launch_decode(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
                           const CUtensorMap& tmV, cudaStream_t stream);
 cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, const CUtensorMap& tmQ, cudaStream_t stream);
+                           const CUtensorMap& tmV, const CUtensorMap& tmQ, const CUtensorMap& tmO,
+                           cudaStream_t stream);
 cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 
 void fill_varlen(const Plan& plan, VarlenSeqs* v);

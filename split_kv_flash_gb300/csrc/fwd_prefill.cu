@@ -79,7 +79,7 @@ template <int HD, class Seqs>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_prefill_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ Seqs seqs) {
+                       const __grid_constant__ CUtensorMap tmO, const __grid_constant__ Seqs seqs) {
     using C = PrefillCfg<HD>;
     constexpr int KST = C::kStagesK;
     constexpr int VST = C::kStagesV;
@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         if (p.q_tma) tma_prefetch_desc(&tmQ);
+        if (p.o_tma) tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -457,6 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
         const bool final_out = (sb == 1);
+        // Final rows go out through the O map: staged as bf16 in Q_t's buffer (the
+        // half's last QK^T, complete once ofinal fired, was its last reader; a
+        // half with no block waits for its Q copy first) and stored by one TMA
+        // copy per 64 columns, coalesced, clipped at the end of the sequence.
+        const bool stage = final_out && p.o_tma;
+        if (stage && cnt == 0 && p.q_tma) {
+            mbar_wait(bar_qfull(t), 0, wc, (kKernPrefill << 8) | kSiteMmaQ);
+        }
 #pragma unroll
         for (int c = 0; c < HD / 16; ++c) {
             float o[16];
@@ -467,7 +476,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] = (cnt >= 1 && l_run > 0.f) ? o[e] * inv : 0.f;
             const int dcol = c * 16;
-            if (row_ok) {
+            if (stage) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(o[2 * e], o[2 * e + 1]);
+                const uint32_t dst = sQt + (c >> 2) * 16384;
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + sw128_offset(r, (2 * c) & 7)),
+                             "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + sw128_offset(r, (2 * c + 1) & 7)),
+                             "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                             : "memory");
+            } else if (row_ok) {
                 if (final_out) {
                     __nv_bfloat16* dst = p.out + ((size_t(b) * p.sq + my.i) * p.Hq + my.h) * HD + dcol;
                     uint4 w0, w1;
@@ -485,6 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[2] = make_float4(o[8], o[9], o[10], o[11]);
                     dst[3] = make_float4(o[12], o[13], o[14], o[15]);
                 }
+            }
+        }
+        if (stage) {
+            fence_proxy_async_smem();
+            named_bar_sync(2 + t, 128);  // the half's 128 threads
+            if (sidx == 0) {
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c)
+                    tma_store_5d(&tmO, sQt + uint32_t(c * 16384), c * 64, 0, ht, (m0 + 128 * t) / p.q_gp, b);
+                bulk_commit_group();
+                bulk_wait_group_read0();  // the source stays valid until the copy has read it
             }
         }
         if (row_ok) {
@@ -506,30 +537,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD, class Seqs>
 cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                       const CUtensorMap& tmQ, const Seqs& seqs, cudaStream_t stream) {
+                       const CUtensorMap& tmQ, const CUtensorMap& tmO, const Seqs& seqs, cudaStream_t stream) {
     using C = PrefillCfg<HD>;
     auto kern = fwd_prefill_kernel<HD, Seqs>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
     return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmK, tmV,
-                      tmQ, seqs);
+                      tmQ, tmO, seqs);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                           const CUtensorMap& tmQ, cudaStream_t stream) {
+                           const CUtensorMap& tmQ, const CUtensorMap& tmO, cudaStream_t stream) {
     if (plan.kBlockM != 128 * kHalves || plan.kBlockN != 128) return cudaErrorInvalidValue;
     if (!plan.varlen) {
         UniformSeqs u{plan.kv_len[0], plan.splits_b[0]};
-        if (plan.d == 128) return launch_one<128, UniformSeqs>(plan, p, tmK, tmV, tmQ, u, stream);
-        return launch_one<64, UniformSeqs>(plan, p, tmK, tmV, tmQ, u, stream);
+        if (plan.d == 128) return launch_one<128, UniformSeqs>(plan, p, tmK, tmV, tmQ, tmO, u, stream);
+        return launch_one<64, UniformSeqs>(plan, p, tmK, tmV, tmQ, tmO, u, stream);
     }
     VarlenSeqs v;
     fill_varlen(plan, &v);
-    if (plan.d == 128) return launch_one<128, VarlenSeqs>(plan, p, tmK, tmV, tmQ, v, stream);
-    return launch_one<64, VarlenSeqs>(plan, p, tmK, tmV, tmQ, v, stream);
+    if (plan.d == 128) return launch_one<128, VarlenSeqs>(plan, p, tmK, tmV, tmQ, tmO, v, stream);
+    return launch_one<64, VarlenSeqs>(plan, p, tmK, tmV, tmQ, tmO, v, stream);
 }
 
 }  // namespace sk

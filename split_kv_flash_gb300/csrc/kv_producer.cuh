@@ -8,8 +8,8 @@
 // thread).
 //
 // The whole producer warp runs these loops (warp-uniform control flow); one
-// elected lane, `leader`, issues the copies.  A ring position counts blocks
-// across the tiles a persistent CTA visits: slot pos % slots, use pos / slots.
+// elected lane, `leader`, issues the copies.  A ring position counts the blocks
+// loaded so far: slot pos % slots, use pos / slots.
 #pragma once
 #include "sm103_ptx.cuh"
 

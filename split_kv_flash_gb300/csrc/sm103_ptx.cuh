@@ -57,25 +57,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe of a phase.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded waits.  Every device-side wait of the kernels goes through here:
 // after `limit_ns` without progress the waiter records `where` in the status
 // word, raises the CTA-wide abort flag and returns false; once the flag is up
-// every later wait returns false at once.  The control flow of the kernels
-// does not depend on the result (only the issuing of copies / MMAs does), so
-// all threads still meet at every CTA barrier and the kernel drains and exits.
+// every later wait on a phase that has not completed returns false at once.
+// The control flow of the kernels does not depend on the result (only the
+// issuing of copies / MMAs does), so all threads still meet at every CTA
+// barrier and the kernel drains and exits.
 struct WaitCtl {
     volatile int* abort_flag;  // shared memory
     uint32_t* status;          // global status word (workspace header)

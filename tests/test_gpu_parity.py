@@ -73,6 +73,9 @@ EDGE = [
     ("prefill_ragged_d128", 2, 4, 2, 128, 200, [333, 200], True, -1),
     ("prefill_ragged_d64", 1, 2, 1, 64, 300, [300], True, -1),
     ("prefill_packed_gqa", 1, 16, 2, 128, 33, [1000], True, -1),
+    # G = 3: a 128-row half is not whole groups of 3 heads, so Q is loaded by the
+    # softmax warps and O stored directly instead of through the TMA maps
+    ("prefill_packed_g3", 1, 6, 2, 128, 40, [500], True, -1),
     ("prefill_local", 1, 4, 4, 128, 520, [520], True, 100),
     ("prefill_window_no_causal", 1, 2, 2, 128, 150, [400], False, 60),
     ("prefill_sk_lt_sq", 1, 2, 2, 128, 260, [100], True, -1),

@@ -17,8 +17,8 @@
 //
 // Blocks are visited from the last one of the range down, so causal and local
 // tiles meet their masked diagonal blocks first; a half whose own range is
-// shorter (the upper rows of a causal tile see one block less) skips the steps
-// outside it.
+// shorter (under a causal mask half 0, the tile's first 128 query rows, sees
+// one block fewer than half 1) skips the steps outside it.
 //
 // Q halves arrive by TMA (a 4-D map whose 128-row box is in packed-row order)
 // unless a half is not whole row groups of that map; then the softmax warps

@@ -255,7 +255,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     fp.rows = p.rows;
     fp.kBlockM = p.kBlockM; fp.kBlockN = p.kBlockN;
     fp.num_m_blocks = p.num_m_blocks; fp.num_splits = p.num_splits; fp.head_tiles = p.head_tiles;
-    fp.flags = p.flags;
+    fp.win = p.win;
     fp.causal = p.causal;
     fp.window_left = p.window_left;
     fp.scale_log2 = float(double(scale) * 1.4426950408889634074);

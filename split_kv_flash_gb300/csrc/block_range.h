@@ -1,16 +1,21 @@
-// block_range.h -- KV block ranges and the CTA -> tile map, shared by the host
-// scheduler (plan.cpp) and the sm_103a kernels so that the device's ranges are
-// bit-identical to the host plan.
+// block_range.h -- which KV blocks a query tile needs, and which tile a CTA of
+// the partial kernel owns.  Shared by the host scheduler (plan.cpp) and the
+// sm_103a kernels, so that the ranges the kernels use are bit-identical to the
+// host plan.
 //
-// FlashAttention tiling strategy and scheduling chapter (分块策略与调度):
-//   section 3.1/3.2 (block.h): causal upper bound on n blocks with the
-//   seqlen_k - seqlen_q offset, local lower bound at window_size_left, PackGQA
-//   rows converted back to query positions before the causal arithmetic;
-//   section 5.3: a split owns ceil(range / count) consecutive blocks, clipped to
-//   the range; the split word holds the split index (low 16 bits) and that
-//   sequence's split count (high 16 bits);
-//   section 4.2/4.4: grid (m blocks, heads x splits, batch) with the m block
-//   index reversed for causal/local work (longest tile first).
+// The rule (FlashAttention tiling strategy and scheduling chapter, section 3:
+// block-level skipping of fully masked blocks; section 5.3: a split's share of
+// the range; section 6.3: packed rows are converted back to query positions
+// before the mask is applied) is derived here from the key interval a tile can
+// see:
+//   * query i sees key j when j <= i + (kv_len - q_len) (causal, bottom-right
+//     aligned) and j >= i + (kv_len - q_len) - window_left (a left window);
+//   * the rows of a tile are ordered by query position, so the union of the
+//     rows' visible keys is [first row's left edge, last row's right edge];
+//   * the tile needs exactly the KV blocks that hold a key of that interval.
+// A split t of S takes ceil(range / S) consecutive blocks starting at
+// t * ceil(range / S), clipped to the range.  Every empty range is reported as
+// [0, 0).
 #pragma once
 #include <stdint.h>
 
@@ -22,68 +27,71 @@
 
 namespace sk {
 
-constexpr int kWindowRightOpen = 1 << 30;  // "no right bound" for a window without causal
-constexpr int kMaxSeqLen = 1 << 29;        // keeps every index below in int32 range
+constexpr int kMaxSeqLen = 1 << 29;  // keeps every index below in int32 range
 
-// Division truncating toward zero, as in the printed C++.
-SK_HD int ceil_div_c(int a, int b) { return (a + b - 1) / b; }
+// Non-negative a, positive b.
+SK_HD int div_up(int a, int b) { return (a + b - 1) / b; }
 SK_HD int imin(int a, int b) { return a < b ? a : b; }
 SK_HD int imax(int a, int b) { return a > b ? a : b; }
 
-struct MaskFlags {
-    bool causal;       // Is_causal of block.h (a causal problem without a window)
-    bool local;        // Is_local of block.h (any problem with a left window)
-    int window_left;
-    int window_right;
+// Which keys a query row sees, relative to its diagonal key i + kv_len - q_len.
+struct KeyWindow {
+    int causal;       // 1: no key after the diagonal
+    int has_left;     // 1: no key more than `left` before the diagonal
+    int left;         // window_left when has_left
 };
 
-// User arguments (causal, window_left) -> block.h flags.  causal with a window
-// is local with right window 0; a window without causal leaves the right open.
-SK_HD MaskFlags mask_flags(int causal, int window_left) {
-    MaskFlags f;
-    f.local = window_left >= 0;
-    f.causal = causal != 0 && !f.local;
-    f.window_left = window_left >= 0 ? window_left : 0;
-    f.window_right = causal ? 0 : kWindowRightOpen;
-    return f;
+SK_HD KeyWindow key_window(int causal, int window_left) {
+    KeyWindow w;
+    w.causal = causal ? 1 : 0;
+    w.has_left = window_left >= 0 ? 1 : 0;
+    w.left = window_left >= 0 ? window_left : 0;
+    return w;
 }
 
 struct BlockRange {
-    int lo, hi;
+    int lo, hi;  // KV blocks [lo, hi); empty ranges are [0, 0)
 };
 
+// Split word of the partial kernel: split index in the low 16 bits, the
+// sequence's split count in the high 16 bits (tiling chapter section 5.3).
 SK_HD uint32_t split_word(int split_idx, int split_count) {
     return (uint32_t(split_count) << 16) | uint32_t(split_idx & 0xFFFF);
 }
 
-// [n_block_min, n_block_max) of one (m block, split) of a sequence.
-SK_HD BlockRange n_block_range(int seqlen_q, int seqlen_k, int m_block, int kBlockM, int kBlockN,
-                               const MaskFlags& f, bool pack_gqa, int G, uint32_t word) {
-    int n_block_max = ceil_div_c(seqlen_k, kBlockN);
-    if (f.causal || f.local) {
-        int m_idx_max = (m_block + 1) * kBlockM;
-        if (pack_gqa) m_idx_max = (m_idx_max - 1) / G + 1;
-        const int n_idx = m_idx_max + seqlen_k - seqlen_q;
-        const int n_idx_right = !f.local ? n_idx : n_idx + f.window_right;
-        n_block_max = imin(n_block_max, ceil_div_c(n_idx_right, kBlockN));
+// KV blocks of `block_keys` keys that rows [tile * tile_rows, (tile + 1) *
+// tile_rows) of a sequence need, cut to the share of split `word`.  With
+// `group` > 1 the rows are packed: row r is query position r / group.
+SK_HD BlockRange tile_key_blocks(int q_len, int kv_len, int tile, int tile_rows, int block_keys,
+                                 const KeyWindow& w, int group, uint32_t word) {
+    const int first_q = (tile * tile_rows) / group;
+    const int last_q = imin((tile * tile_rows + tile_rows - 1) / group, q_len - 1);
+    const int shift = kv_len - q_len;  // query i's diagonal key is i + shift
+    int begin = 0;
+    int end = div_up(kv_len, block_keys);
+    if (w.causal) {
+        const int last_key = last_q + shift;
+        end = last_key < 0 ? 0 : imin(end, last_key / block_keys + 1);
     }
-    int n_block_min = 0;
-    if (f.local) {
-        int m_idx_min = m_block * kBlockM;
-        if (pack_gqa) m_idx_min = m_idx_min / G;
-        const int n_idx = m_idx_min + seqlen_k - seqlen_q;
-        const int n_idx_left = n_idx - f.window_left;
-        n_block_min = imax(0, n_idx_left / kBlockN);
+    if (w.has_left) {
+        const int first_key = first_q + shift - w.left;
+        if (first_key > 0) begin = first_key / block_keys;
     }
-    const int split_idx = int(word & 0xFFFF);
-    const int split_cnt = int(word >> 16);
-    const int per = ceil_div_c(n_block_max - n_block_min, split_cnt);
-    n_block_min = n_block_min + split_idx * per;
-    n_block_max = imin(n_block_min + per, n_block_max);
-    return {n_block_min, n_block_max};
+    if (end <= begin) return {0, 0};
+    const int count = int(word >> 16);
+    const int idx = int(word & 0xFFFF);
+    const int share = div_up(end - begin, count);
+    const int lo = begin + idx * share;
+    const int hi = imin(lo + share, end);
+    if (hi <= lo) return {0, 0};
+    return {lo, hi};
 }
 
-// Which tile one CTA of the partial kernel owns.
+// Which tile one CTA of the partial kernel owns.  Grid (m blocks, head tiles x
+// splits, sequences), x fastest (tiling chapter section 4.2).  With causal or
+// windowed masks the m block index runs backwards, so the CTAs launched first
+// own the tiles with the most KV blocks (longest processing time first,
+// section 4.4).
 struct TileCoord {
     int m_block, head_tile, split, batch;
 };

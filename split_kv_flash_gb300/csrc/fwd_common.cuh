@@ -38,7 +38,7 @@ struct FwdParams {
     int pack_gqa;
     int rows;          // packed rows per head tile
     int kBlockM, kBlockN, num_m_blocks, num_splits, head_tiles;
-    MaskFlags flags;   // block-level flags
+    KeyWindow win;     // which keys a row sees (block ranges)
     int causal;        // element-level mask
     int window_left;   // < 0: none
     float scale_log2;  // softmax scale * log2(e)

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sk = seqs.seq_len(b);
     const int kv_off = seqs.seq_off(b);
     const BlockRange br =
-        n_block_range(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.flags, p.pack_gqa != 0, p.G, word);
+        tile_key_blocks(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.win, p.pack_gqa ? p.G : 1, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
     const int m0 = tc.m_block * p.kBlockM;
     const int rows_valid = min(p.kBlockM, p.rows - m0);

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sk = seqs.seq_len(b);
     const int kv_off = seqs.seq_off(b);
     const BlockRange br =
-        n_block_range(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.flags, p.pack_gqa != 0, p.G, word);
+        tile_key_blocks(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.win, p.pack_gqa ? p.G : 1, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
     const int kvh = p.pack_gqa ? ht : ht / p.G;
     const int m0 = tc.m_block * (128 * kHalves);
@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < kHalves; ++t) {
         rows_h[t] = max(0, min(128, p.rows - (m0 + 128 * t)));
-        const BlockRange hr = n_block_range(p.sq, sk, tc.m_block * kHalves + t, 128, p.kBlockN, p.flags,
-                                            p.pack_gqa != 0, p.G, split_word(0, 1));
+        const BlockRange hr = tile_key_blocks(p.sq, sk, tc.m_block * kHalves + t, 128, p.kBlockN, p.win,
+                                              p.pack_gqa ? p.G : 1, split_word(0, 1));
         const int lo = max(hr.lo, br.lo), hi = min(hr.hi, br.hi);
         count[t] = (rows_h[t] > 0 && hi > lo) ? hi - lo : 0;
         first[t] = count[t] > 0 ? br.hi - hi : 0;

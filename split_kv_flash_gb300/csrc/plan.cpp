@@ -19,16 +19,22 @@ constexpr long long kL2SplitBytes = 50LL * 1024 * 1024;
 
 }  // namespace
 
-// Tiling chapter section 6.2 (should_pack_gqa): efficiency = useful rows / rows
-// rounded up to block_m; pack when the unpacked efficiency is below 0.9 of the
-// packed one.  float ratios against a double constant, as printed.
+// PackGQA decision (tiling chapter section 6.2).  A tile's "fill" is the share
+// of its rows that hold real queries once the rows are padded to whole tiles,
+// in binary32 as the chapter defines it.  Packing G heads into the rows pays
+// when the unpacked fill falls below 0.9 of the packed one.  Sequences of
+// different query lengths always pack.
+namespace {
+float tile_fill(int rows, int tile_rows) {
+    const int padded = div_up(rows, tile_rows) * tile_rows;
+    return float(rows) / float(padded);
+}
+}  // namespace
+
 bool should_pack_gqa(bool varlen_q, int seqlen_q, int qhead_per_khead, int block_m) {
     if (varlen_q) return true;
-    auto round_up = [](int a, int b) { return (a + b - 1) / b * b; };
-    const float nopack = float(seqlen_q) / float(round_up(seqlen_q, block_m));
-    const int packed = seqlen_q * qhead_per_khead;
-    const float pack = float(packed) / float(round_up(packed, block_m));
-    return nopack < 0.9 * pack;
+    const double packed_fill = tile_fill(seqlen_q * qhead_per_khead, block_m);
+    return tile_fill(seqlen_q, block_m) < 0.9 * packed_fill;
 }
 
 // Tiling chapter section 5.2 (num_splits_heuristic): fill gate at 0.8 * SMs,
@@ -61,11 +67,11 @@ int num_splits_fa_heuristic(int total_mblocks, int num_sms, int num_n_blocks, in
 std::vector<int> per_sequence_splits(const std::vector<int>& kv_len, int block_n, int num_splits) {
     std::vector<int> out(kv_len.size(), 1);
     int nmax = 0;
-    for (int s : kv_len) nmax = std::max(nmax, ceil_div_c(s, block_n));
+    for (int s : kv_len) nmax = std::max(nmax, div_up(s, block_n));
     if (num_splits <= 1 || nmax == 0) return out;
-    const int chunk = ceil_div_c(nmax, num_splits);
+    const int chunk = div_up(nmax, num_splits);
     for (size_t b = 0; b < kv_len.size(); ++b)
-        out[b] = std::max(1, ceil_div_c(ceil_div_c(kv_len[b], block_n), chunk));
+        out[b] = std::max(1, div_up(div_up(kv_len[b], block_n), chunk));
     return out;
 }
 
@@ -87,8 +93,8 @@ int fill_policy(const Plan& p, int capacity, int max_splits) {
         if (ctas <= capacity) { best = S; break; }
     }
     // drop splits that would only repeat the same chunk size
-    const int chunk = ceil_div_c(p.nblk_max, best);
-    return ceil_div_c(p.nblk_max, chunk);
+    const int chunk = div_up(p.nblk_max, best);
+    return div_up(p.nblk_max, chunk);
 }
 
 }  // namespace
@@ -123,7 +129,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.sq = q_len; p.d = d;
     p.causal = causal ? 1 : 0;
     p.window_left = window_left < 0 ? -1 : window_left;
-    p.flags = mask_flags(p.causal, p.window_left);
+    p.win = key_window(p.causal, p.window_left);
     p.kv_len.assign(kv_len_host, kv_len_host + B);
     p.kv_off.assign(size_t(B) + 1, 0);
     long long total = 0;
@@ -167,8 +173,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
         // Prefill kernel: 256-row tiles, two 128-row halves that share each K/V block.
         p.kBlockM = 256;
     }
-    p.num_m_blocks = p.rows == 0 ? 0 : ceil_div_c(p.rows, p.kBlockM);
-    p.nblk_max = ceil_div_c(p.max_kv, p.kBlockN);
+    p.num_m_blocks = p.rows == 0 ? 0 : div_up(p.rows, p.kBlockM);
+    p.nblk_max = div_up(p.max_kv, p.kBlockN);
     p.reverse_m = p.causal || p.window_left >= 0;
 
     // Split count.
@@ -189,7 +195,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
                 break;
             }
             case SK_POLICY_FIXED_CHUNK:
-                S = std::max(1, std::min(32, ceil_div_c(p.max_kv, 2048)));
+                S = std::max(1, std::min(32, div_up(p.max_kv, 2048)));
                 break;
             case SK_POLICY_MIN_CHUNK: {
                 const int fill = int(std::min<long long>(
@@ -246,9 +252,9 @@ void plan_ranges(const Plan& p, int32_t* out) {
                     e[0] = 0; e[1] = 0; e[2] = int32_t(word); e[3] = 0;
                     continue;
                 }
-                const BlockRange r = n_block_range(p.sq, p.kv_len[size_t(t.batch)], t.m_block,
-                                                   p.kBlockM, p.kBlockN, p.flags, p.pack_gqa, p.G,
-                                                   word);
+                const BlockRange r = tile_key_blocks(p.sq, p.kv_len[size_t(t.batch)], t.m_block,
+                                                     p.kBlockM, p.kBlockN, p.win, p.pack_gqa ? p.G : 1,
+                                                     word);
                 e[0] = r.lo; e[1] = r.hi; e[2] = int32_t(word); e[3] = 1;
             }
 }

@@ -20,7 +20,7 @@ struct Plan {
     // problem
     int B = 0, Hq = 0, Hkv = 0, G = 1, sq = 0, d = 0;
     int causal = 0, window_left = -1;
-    MaskFlags flags{};
+    KeyWindow win{};
     bool varlen = false;       // kv lengths differ between sequences
     std::vector<int> kv_len;   // [B]
     std::vector<long long> kv_off;  // [B + 1]

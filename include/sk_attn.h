@@ -71,7 +71,7 @@ typedef enum {
 typedef enum {
     SK_PATH_AUTO = 0,
     SK_PATH_DECODE = 1,   /* <= 64 packed query rows per tile: KV rows on the MMA M axis */
-    SK_PATH_PREFILL = 2   /* 128 query rows per tile: query rows on the MMA M axis */
+    SK_PATH_PREFILL = 2   /* 256-row tiles: two 128-row halves that share each K/V block; query rows on the MMA M axis */
 } sk_path;
 
 /* Options; an all-zero struct (or NULL) selects the defaults. */
@@ -171,12 +171,24 @@ sk_status sk_attn_workspace_status(void* workspace, void* cuda_stream, int* wher
  *     on cuda_stream) before the kernels.  Calls whose work overlaps on the GPU
  *     (different streams, or several host threads without ordering) race on the
  *     scratch and give wrong results: order them on one stream.
- *   - Device-side wait timeouts are not reported through this entry point. */
+ *   - A kernel that gives up on a bounded wait leaves its code in the built-in
+ *     scratch; read it with sk_attn_noalloc_status before the next call on the
+ *     device (which clears it).
+ *   - The cached address belongs to the device's current context: after
+ *     cudaDeviceReset the library must be reloaded before this entry point is
+ *     used again. */
 #define SK_NOALLOC_SCRATCH_BYTES (16u << 20)
 sk_status sk_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                               int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
                               float scale, int causal, int window_left, void* cuda_stream,
                               const sk_attn_opts* opts);
+
+/* sk_attn_workspace_status for the built-in scratch of sk_attn_fwd_noalloc on
+ * the current device: synchronises cuda_stream, returns SK_OK or
+ * SK_ERR_DEVICE_TIMEOUT (then clears the word; *where, optional, receives the
+ * code of the wait that expired).  The pages have no counterpart to this entry
+ * point either; it lets callers of sk_attn_fwd_noalloc see device timeouts. */
+sk_status sk_attn_noalloc_status(void* cuda_stream, int* where);
 
 const char* sk_attn_status_string(sk_status s);
 /* One-line reason for the last error returned on this thread ("" if none). */

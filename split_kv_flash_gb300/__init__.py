@@ -14,7 +14,7 @@ import os
 __all__ = [
     "SKError", "Opts", "PlanInfo", "lib", "sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd",
     "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_status_string",
-    "sk_attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "sk_attn_fwd_noalloc", "sk_attn_noalloc_status", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
     "SK_PATH_PREFILL", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
@@ -90,8 +90,9 @@ def lib():
                                           vp, ctypes.POINTER(Opts)]
         L.sk_attn_read_plan_echo.argtypes = [vp, _i32p, sz, vp]
         L.sk_attn_workspace_status.argtypes = [vp, vp, _intp]
+        L.sk_attn_noalloc_status.argtypes = [vp, _intp]
         for f in ("sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd", "sk_attn_fwd_noalloc",
-                  "sk_attn_read_plan_echo", "sk_attn_workspace_status"):
+                  "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_noalloc_status"):
             getattr(L, f).restype = ci
         L.sk_attn_status_string.argtypes = [ci]
         L.sk_attn_status_string.restype = ctypes.c_char_p
@@ -103,8 +104,13 @@ def lib():
     return _lib
 
 
-def _kv_array(kv_len):
+def _kv_array(kv_len, B=None):
+    """kv_len as a C int array; with B given, it must hold exactly B lengths
+    (the library reads kv_len[0 .. B-1]; B <= 0 is left to the library to
+    reject)."""
     vals = [int(x) for x in kv_len]
+    if B is not None and int(B) > 0 and len(vals) != int(B):
+        raise ValueError("kv_len holds %d lengths for B = %d sequences" % (len(vals), int(B)))
     return (ctypes.c_int * max(len(vals), 1))(*vals), len(vals)
 
 
@@ -134,7 +140,7 @@ def sk_attn_version():
 
 
 def sk_attn_plan(B, Hq, Hkv, q_len, kv_len, d, causal=False, window_left=-1, opts=None):
-    arr, _ = _kv_array(kv_len)
+    arr, _ = _kv_array(kv_len, B)
     info = PlanInfo()
     _check(lib().sk_attn_plan(B, Hq, Hkv, q_len, arr, d, int(causal), int(window_left),
                               ctypes.byref(opts) if opts is not None else None, ctypes.byref(info)))
@@ -146,7 +152,7 @@ def sk_attn_plan_ranges(B, Hq, Hkv, q_len, kv_len, d, causal=False, window_left=
     info = sk_attn_plan(B, Hq, Hkv, q_len, kv_len, d, causal, window_left, opts)
     n = int(info.num_ctas) * 4
     buf = (ctypes.c_int32 * max(n, 1))()
-    arr, _ = _kv_array(kv_len)
+    arr, _ = _kv_array(kv_len, B)
     _check(lib().sk_attn_plan_ranges(B, Hq, Hkv, q_len, arr, d, int(causal), int(window_left),
                                      ctypes.byref(opts) if opts is not None else None, buf, n))
     return [tuple(buf[i:i + 4]) for i in range(0, n, 4)]
@@ -156,7 +162,7 @@ def sk_attn_fwd(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len, d, scale, causal, 
                 workspace, ws_bytes, stream=None, opts=None):
     """Pointer-level call: q, k, v, out, lse, workspace are device pointers (ints)
     or tensors; stream is a cudaStream_t handle (int) or a torch.cuda.Stream."""
-    arr, _ = _kv_array(kv_len)
+    arr, _ = _kv_array(kv_len, B)
     if stream is not None and not isinstance(stream, int):
         stream = stream.cuda_stream
     _check(lib().sk_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, q_len,
@@ -172,12 +178,22 @@ def sk_attn_fwd_noalloc(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len, d, scale, 
     (NOALLOC_SCRATCH_BYTES per GPU) is used instead; larger problems raise
     SKError(SK_ERR_WORKSPACE_TOO_SMALL).  Calls that overlap on the GPU share
     that scratch and race: keep them ordered on one stream."""
-    arr, _ = _kv_array(kv_len)
+    arr, _ = _kv_array(kv_len, B)
     if stream is not None and not isinstance(stream, int):
         stream = stream.cuda_stream
     _check(lib().sk_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
                                      q_len, arr, d, float(scale), int(causal), int(window_left),
                                      stream, ctypes.byref(opts) if opts is not None else None))
+
+
+def sk_attn_noalloc_status(stream=None):
+    """Status word left by the last sk_attn_fwd_noalloc call on the current
+    device: returns (status, where) like sk_attn_workspace_status."""
+    where = ctypes.c_int(0)
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    st = lib().sk_attn_noalloc_status(stream, ctypes.byref(where))
+    return st, where.value
 
 
 def sk_attn_read_plan_echo(workspace, num_ctas, stream=None):

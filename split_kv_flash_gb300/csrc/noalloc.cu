@@ -90,3 +90,14 @@ extern "C" sk_status sk_attn_fwd_noalloc(const void* q, const void* k, const voi
     return sk_attn_fwd(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len_host, d, scale, causal,
                        window_left, scratch, kNoallocScratchBytes, cuda_stream, opts);
 }
+
+// Status of the last sk_attn_fwd_noalloc call on this device: the same word
+// sk_attn_workspace_status reads from a caller workspace, here in the built-in
+// scratch.  Read it before the next sk_attn_fwd_noalloc call, which clears it.
+extern "C" sk_status sk_attn_noalloc_status(void* cuda_stream, int* where) {
+    if (where) *where = 0;
+    void* scratch = nullptr;
+    sk_status s = scratch_address(&scratch);
+    if (s != SK_OK) return s;
+    return sk_attn_workspace_status(scratch, cuda_stream, where);
+}

@@ -107,3 +107,18 @@ def test_fwd_without_gpu_fails_cleanly(sk):
     with pytest.raises(sk.SKError) as ei:
         sk.sk_attn_fwd(16, 16, 16, 16, 16, 1, 4, 4, 1, [256], 64, 0.125, 0, -1, 256, 1 << 20)
     assert ei.value.status in (2, 5)
+
+
+def test_binding_checks_kv_len_length(sk):
+    """The C side reads kv_len[0 .. B-1]; the binding refuses a list of another
+    length before any call reaches the library."""
+    o = _opts(sk)
+    with pytest.raises(ValueError):
+        sk.sk_attn_plan(3, 4, 4, 1, [100, 200], 128, opts=o)
+    with pytest.raises(ValueError):
+        sk.sk_attn_plan_ranges(1, 4, 4, 1, [100, 200], 128, opts=o)
+    with pytest.raises(ValueError):
+        sk.sk_attn_fwd(0, 0, 0, 0, 0, 2, 4, 4, 1, [100], 128, 0.1, 0, -1, 0, 0)
+    with pytest.raises(ValueError):
+        sk.sk_attn_fwd_noalloc(0, 0, 0, 0, 0, 2, 4, 4, 1, [100, 1, 2], 128, 0.1, 0, -1)
+    assert sk.sk_attn_plan(2, 4, 4, 1, [100, 200], 128, opts=o).num_ctas >= 2

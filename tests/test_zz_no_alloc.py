@@ -68,3 +68,29 @@ def test_noalloc_rejects_problems_larger_than_the_scratch(sk):
         sk.sk_attn_fwd_noalloc(q, k, k, out, lse, B, Hq, Hkv, sq, kv, d, 0.1, 0, -1, None, opts)
     assert ei.value.status == 3
     assert "scratch" in sk.sk_attn_last_error()
+
+
+def test_noalloc_reports_a_device_timeout_and_recovers(sk):
+    """A kernel wait that nothing signals gives up after the bounded wait; the
+    code it leaves in the built-in scratch is read with sk_attn_noalloc_status,
+    and the next call on the same scratch is correct again."""
+    w = wl.gqa_decode(16384)
+    q, k, v = wl.make_inputs(w)
+    qg, kg, vg = H.to_gpu(q, k, v)
+    stream = torch.cuda.current_stream()
+    opts = sk.Opts()
+    opts.debug_inject_stall = 1
+    opts.wait_timeout_us = 20000
+    out = torch.empty((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device="cuda")
+    sk.sk_attn_fwd_noalloc(qg, kg, vg, out, lse, w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d,
+                           w.scale, 0, -1, stream, opts)
+    st, where = sk.sk_attn_noalloc_status(stream)
+    assert st == 6 and (where & 0xFF) == 8, (st, where)
+    assert sk.sk_attn_noalloc_status(stream)[0] == 0  # read once, then cleared
+    ref_out, ref_lse, _ = sk.attn_fwd(qg, kg, vg, w.kv_len, w.scale)
+    out, lse = _noalloc(sk, w, qg, kg, vg, stream)
+    torch.cuda.synchronize()
+    assert sk.sk_attn_noalloc_status(stream)[0] == 0
+    assert (out.float() - ref_out.float()).abs().max().item() <= H.TOL_O
+    assert (lse - ref_lse).abs().max().item() <= H.TOL_LSE

@@ -40,10 +40,10 @@ METRIC = "decode attn HBM GB/s (% of peak) and prefill TFLOP/s (% of peak), 1 GB
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
-# The partial kernel is bracketed by CUDA events on every 16th timed step only:
+# The partial kernel is bracketed by CUDA events on every 4th timed step only:
 # an event between the partial and the combine kernel keeps the combine from
 # being launched early (programmatic dependent launch), so most steps run without.
-EVENT_EVERY = 16
+EVENT_EVERY = 4
 
 
 def parse():
@@ -350,61 +350,156 @@ def gpu_prefill(sk, w, steps, warmup, device):
 
 
 def sweep_workloads():
-    """The other configurations, one representative set each (tiny decode, the
-    other GQA decode lengths, speculative verify, varlen decode)."""
+    """Every other configuration: tiny decode, the other GQA decode lengths,
+    speculative verify (q_len 9 / 17 / 33 x prefix 128 / 512 / 2048 / 8192) and
+    varlen decode (B = 1 ... 32)."""
     ws = [wl.tiny_decode()]
     ws += [wl.gqa_decode(kv) for kv in (4096, 16384, 32768)]
-    ws += [wl.spec_verify(q, 8192) for q in (9, 17, 33)] + [wl.spec_verify(17, 2048)]
-    ws += [wl.varlen_decode(b) for b in (1, 8, 32)]
+    ws += [wl.spec_verify(q, p) for q in (9, 17, 33) for p in (128, 512, 2048, 8192)]
+    ws += [wl.varlen_decode(b) for b in (1, 2, 4, 8, 16, 32)]
     return ws
 
 
-def gpu_sweep(sk, device, hbm_peak, reps=20, warmup=3):
-    """Whole-call time (partial + combine, CUDA events on the stream around the
-    call) per configuration, L2 flushed before every timed call.  Inputs are
-    drawn on the device (throughput does not depend on the values; parity is
-    tested on the seeded CPU draws)."""
+def short_name(n):
+    """Short key for a workload name (flat keys of the bench line)."""
+    n = n.replace("gqa_decode_b1_hq32_hkv4_d128_", "gqa_").replace("verify_b2_h16_d128_", "verify_")
+    n = n.replace("varlen_decode_", "varlen_").replace("_hq32_hkv8_d128", "")
+    return n.replace("tiny_decode_b1_h4_d64_kv256", "tiny")
+
+
+def gpu_sweep(sk, device, hbm_peak, reps=20, warmup=3, loop_reps=10):
+    """Per configuration, two timings of whole calls (partial + combine):
+      - "us": one call at a time, CUDA events on the stream around it, L2
+        flushed before each call (includes the launch latency of a lone call);
+      - "loop_us": calls back to back as a decode loop issues them, replayed
+        from a CUDA graph over rotating copies of the inputs that together
+        exceed twice the L2 size (so every call reads HBM), time per call.
+    Inputs are drawn on the device (throughput does not depend on the values;
+    parity is tested on the seeded CPU draws)."""
     rows = []
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     for w in sweep_workloads():
+        nbytes = decode_bytes(w)
+        kv_bytes = 2 * w.total_kv * w.Hkv * w.d * 2
+        R = max(1, min(4096, -(-2 * L2_BYTES // max(kv_bytes, 1))))
         g = torch.Generator(device=device).manual_seed(w.seed)
-        q = torch.randn((w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
-        k = (torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g) * w.k_scale).to(torch.bfloat16)
-        v = torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g).to(torch.bfloat16)
-        out = torch.empty((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device=device)
-        lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
+        q = torch.randn((R, w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
+        k = (torch.randn((R, w.total_kv, w.Hkv, w.d), device=device, generator=g) * w.k_scale).to(torch.bfloat16)
+        v = torch.randn((R, w.total_kv, w.Hkv, w.d), device=device, generator=g).to(torch.bfloat16)
+        out = torch.empty((R, w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((R, w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
         info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left)
         wsb = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
 
-        def call():
-            sk.sk_attn_fwd(q, k, v, out, lse, w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.scale,
-                           w.causal, w.window_left, wsb, wsb.numel(), stream)
+        def call(r, st):
+            sk.sk_attn_fwd(q[r], k[r], v[r], out[r], lse[r], w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d,
+                           w.scale, w.causal, w.window_left, wsb, wsb.numel(), st)
 
-        for _ in range(warmup):
-            call()
+        for i in range(warmup):
+            call(i % R, stream)
         evb = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
         eve = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
         for i in range(reps):
             flush.fill_(float(i))
             evb[i].record(stream)
-            call()
+            call(i % R, stream)
             eve[i].record(stream)
         torch.cuda.synchronize(device)
         st, where = sk.sk_attn_workspace_status(wsb)
         if st != 0:
             raise RuntimeError("device status %d at %d (%s)" % (st, where, w.name))
         ms = statistics.median(evb[i].elapsed_time(eve[i]) for i in range(reps))
-        nbytes = decode_bytes(w)
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        row = {"workload": w.name, "us": ms * 1e3, "bytes": nbytes, "gbs": gbs,
-               "frac_of_hbm_peak": gbs / hbm_peak, "path": "decode" if info.path == 1 else "prefill",
-               "splits": info.num_splits, "ctas": info.num_ctas}
+        row = {"workload": w.name, "us": ms * 1e3, "bytes": nbytes,
+               "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+               "path": "decode" if info.path == 1 else "prefill", "splits": info.num_splits,
+               "ctas": info.num_ctas, "rotating_copies": R}
+        loop_ms = None
+        try:
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                call(0, side)  # warm the side stream outside the capture
+            torch.cuda.synchronize(device)
+            with torch.cuda.graph(graph, stream=side):
+                for r in range(R):
+                    call(r, side)
+            graph.replay()
+            torch.cuda.synchronize(device)
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(loop_reps):
+                graph.replay()
+            t1.record(stream)
+            torch.cuda.synchronize(device)
+            loop_ms = t0.elapsed_time(t1) / (loop_reps * R)
+            del graph
+        except Exception as e:  # noqa: BLE001 - report, keep the isolated numbers
+            row["loop_error"] = str(e)[:200]
+        st, where = sk.sk_attn_workspace_status(wsb)
+        if st != 0:
+            raise RuntimeError("device status %d at %d (%s, loop)" % (st, where, w.name))
+        if loop_ms is not None:
+            row["loop_us"] = loop_ms * 1e3
+            row["loop_frac_of_hbm_peak"] = nbytes / (loop_ms * 1e-3) / 1e9 / hbm_peak
         if w.q_len > 1:
             row["tflops"] = prefill_flops(w) / (ms * 1e-3) / 1e12
         rows.append(row)
         del q, k, v, out, lse, wsb
+        torch.cuda.empty_cache()
     return rows
+
+
+def sweep_summary(rows):
+    """Flat scalars (per workload: isolated and loop microseconds and fractions
+    of the HBM peak), plus the worst row of each kind."""
+    flat = {}
+    for r in rows:
+        n = short_name(r["workload"])
+        flat[n + "_us"] = round(r["us"], 2)
+        flat[n + "_frac"] = round(r["frac_of_hbm_peak"], 4)
+        if "loop_us" in r:
+            flat[n + "_loop_us"] = round(r["loop_us"], 2)
+            flat[n + "_loop_frac"] = round(r["loop_frac_of_hbm_peak"], 4)
+    worst = min(rows, key=lambda r: r["frac_of_hbm_peak"])
+    flat["worst_workload"] = worst["workload"]
+    flat["worst_frac"] = round(worst["frac_of_hbm_peak"], 4)
+    loops = [r for r in rows if "loop_frac_of_hbm_peak" in r]
+    if loops:
+        wl_ = min(loops, key=lambda r: r["loop_frac_of_hbm_peak"])
+        flat["worst_loop_workload"] = wl_["workload"]
+        flat["worst_loop_frac"] = round(wl_["loop_frac_of_hbm_peak"], 4)
+    return flat
+
+
+def host_cost_us(sk, device, calls=2000):
+    """Host time of one sk_attn_fwd call through the C ABI (median over calls;
+    plan, tensor maps and launches; GPU work is asynchronous).  GQA decode at
+    16384 keys, one set of inputs."""
+    import ctypes
+    w = wl.gqa_decode(16384)
+    q = torch.zeros((w.B, w.q_len, w.Hq, w.d), dtype=torch.bfloat16, device=device)
+    k = torch.zeros((w.total_kv, w.Hkv, w.d), dtype=torch.bfloat16, device=device)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d)
+    wsb = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
+    L = sk.lib()
+    arr, _ = sk._kv_array(w.kv_len, w.B)
+    sh = torch.cuda.current_stream(device).cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), k.data_ptr(), out.data_ptr(), lse.data_ptr(), w.B, w.Hq, w.Hkv,
+            w.q_len, arr, w.d, ctypes.c_float(w.scale), 0, -1, wsb.data_ptr(), wsb.numel(), sh, None)
+    ts = []
+    for i in range(calls):
+        t0 = time.perf_counter()
+        L.sk_attn_fwd(*args)
+        ts.append(time.perf_counter() - t0)
+        if i % 64 == 63:
+            torch.cuda.synchronize(device)  # keep the launch queue short
+    torch.cuda.synchronize(device)
+    return statistics.median(ts) * 1e6
 
 
 _pg = None
@@ -432,10 +527,10 @@ def whole_job_gbs(bytes_per_step_per_rank, steps, world, local_ms):
 
 
 # ----------------------------------------------------------------- CPU arm
-def cpu_oracle(w, seconds, rows_per_call=None):
-    """Time the fp64 oracle on the host cores on whole query rows of w: each
-    call computes `rows_per_call` (b, h, i) rows; value in GB/s of the
-    algorithmic bytes those rows stand for."""
+def cpu_oracle(w, seconds, rows_per_call=None, threads=None):
+    """Time the fp64 oracle on the host cores (all of them unless `threads`) on
+    whole query rows of w: each call computes `rows_per_call` (b, h, i) rows;
+    value in GB/s of the algorithmic bytes those rows stand for."""
     import oracle
     q, k, v = wl.make_inputs(w)
     qb, kb, vb = wl.bits(q), wl.bits(k), wl.bits(v)
@@ -443,7 +538,7 @@ def cpu_oracle(w, seconds, rows_per_call=None):
                         dtype=np.int32)
     n = rows_per_call or len(all_rows)
     rows = all_rows[:n]
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     oracle.attn_rows(qb, kb, vb, w.kv_len, w.scale, rows[:1], w.causal, w.window_left, threads)
     t0 = time.perf_counter()
     calls = 0
@@ -565,27 +660,37 @@ def main():
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": ms, "steps": e2e_steps}
     if not args.no_prefill:
-        pre = {}
+        # Flat scalars only, so that every number survives in a parsed record.
+        pre = {"unit": "TFLOP/s", "peak": bf16_peak, "peak_source": peak_src + " bf16_tflops (burst)",
+               "flop_count": "4 * d per visible (query, key) pair per head"}
         for local_w in (False, True):
             pw = wl.prefill(local_w)
             ms, pinfo = gpu_prefill(sk, pw, 10, 3, device)
             fl = prefill_flops(pw)
             tf = fl / (ms * 1e-3) / 1e12
             key = "local1024" if local_w else "causal"
-            pre[key] = {"workload": pw.name, "tflops": tf, "ms": ms, "flops": fl,
-                        "frac_of_bf16_peak": tf / bf16_peak}
-        result["prefill"] = {
-            "unit": "TFLOP/s", "peak": bf16_peak, "peak_source": peak_src + " bf16_tflops (burst)",
-            "flop_count": "4 * d per visible (query, key) pair per head", **pre,
-            "traffic": ncu_traffic("prefill_causal_8192", PREFILL_SOURCES)}
+            pre[key + "_workload"] = pw.name
+            pre[key + "_tflops"] = tf
+            pre[key + "_ms"] = ms
+            pre[key + "_flops"] = fl
+            pre[key + "_frac_of_bf16_peak"] = tf / bf16_peak
+        pre["traffic"] = ncu_traffic("prefill_causal_8192", PREFILL_SOURCES)
+        result["prefill"] = pre
     if rank == 0 and not args.no_sweep:
+        rows = gpu_sweep(sk, device, hbm_peak)
         result["sweep"] = {
-            "unit": "GB/s", "peak": hbm_peak, "bound": "hbm",
-            "method": "median of 20 whole calls (partial + combine), CUDA events on the stream, "
-                      "L2 flushed before each call; bytes = K + V of every sequence + Q + O + LSE",
-            "rows": gpu_sweep(sk, device, hbm_peak)}
+            "unit": "us and fraction of the HBM peak", "peak": hbm_peak, "bound": "hbm",
+            "method": "us: median of 20 lone calls (partial + combine), CUDA events around each, L2 "
+                      "flushed before each; loop_us: calls back to back from a CUDA graph over rotating "
+                      "inputs larger than 2x L2. bytes = K + V of every sequence + Q + O + LSE",
+            **sweep_summary(rows)}
+        result["sweep_rows"] = rows
+        result["host_us_per_call"] = host_cost_us(sk, device)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)
+        one = cpu_oracle(w, max(2.0, args.cpu_seconds / 4), rows_per_call=4, threads=1)
+        result["cpu_baseline"]["single_core_value"] = one["value"]
+        result["cpu_baseline"]["single_core_sample"] = one["sample"]
     if rank == 0:
         print(json.dumps(result), flush=True)
     if _pg is not None:

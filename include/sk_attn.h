@@ -34,9 +34,10 @@
  *     memory and keeps no per-call state.  Inputs are never written.
  *   - Errors are returned before any launch; no output is partly written by a
  *     call that returns an error.  sk_attn_last_error() gives a one-line reason.
- *   - Every K/V element that a kernel stages must be finite (the rows of the next
- *     sequence that share a 128-row block with the end of a sequence are loaded
- *     and then masked).
+ *   - Rows outside a sequence never affect its result.  The 128-row block that
+ *     holds the end of a sequence also holds the first rows of the next one:
+ *     their scores are masked and their V rows are zeroed in shared memory
+ *     before they are multiplied, so Inf or NaN there cannot leak in.
  */
 #ifndef SK_ATTN_H
 #define SK_ATTN_H

@@ -93,7 +93,7 @@ bool make_o_map(CUtensorMap* m, void* o, int B, int q_len, int Hq, int d, int gp
 }
 
 struct DeviceInfo {
-    int sms = 0, major = 0, minor = 0;
+    int dev = 0, sms = 0, major = 0, minor = 0;
 };
 
 sk_status current_device(DeviceInfo* di) {
@@ -109,6 +109,7 @@ sk_status current_device(DeviceInfo* di) {
         return SK_OK;
     }
     DeviceInfo d;
+    d.dev = dev;
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
@@ -122,6 +123,60 @@ sk_status current_device(DeviceInfo* di) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- per-thread cache of plans and tensor maps
+struct CallKey {
+    int dev, B, Hq, Hkv, q_len, d, causal, window_left;
+    int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms;
+    const void *q, *k, *v, *out;
+};
+
+struct CallEntry {
+    CallKey key;
+    Plan plan;  // plan.kv_len holds the lengths the entry was made for
+    CUtensorMap tmK, tmV, tmQ, tmO;
+    bool q_tma = false, o_tma = false;
+    int q_gp = 1;
+};
+
+constexpr int kCallCacheSize = 64;
+
+struct CallCache {
+    CallEntry entries[kCallCacheSize];
+    bool used[kCallCacheSize] = {};
+    int next = 0;   // round-robin replacement
+    int last = -1;  // most recent hit or insert, checked first
+};
+
+thread_local CallCache g_calls;
+
+bool same_call(const CallEntry& e, const CallKey& k, const int* kv_len) {
+    if (memcmp(&e.key, &k, sizeof k) != 0) return false;
+    return memcmp(e.plan.kv_len.data(), kv_len, sizeof(int) * size_t(k.B)) == 0;
+}
+
+const CallEntry* lookup_call(const CallKey& k, const int* kv_len) {
+    CallCache& c = g_calls;
+    if (k.B <= 0) return nullptr;
+    if (c.last >= 0 && c.used[c.last] && same_call(c.entries[c.last], k, kv_len)) return &c.entries[c.last];
+    for (int i = 0; i < kCallCacheSize; ++i)
+        if (c.used[i] && same_call(c.entries[i], k, kv_len)) {
+            c.last = i;
+            return &c.entries[i];
+        }
+    return nullptr;
+}
+
+const CallEntry* insert_call(const CallKey& k, CallEntry&& e) {
+    CallCache& c = g_calls;
+    const int i = c.next;
+    c.next = (c.next + 1) % kCallCacheSize;
+    c.entries[i] = std::move(e);
+    c.entries[i].key = k;
+    c.used[i] = true;
+    c.last = i;
+    return &c.entries[i];
+}
 
 }  // namespace
 
@@ -200,44 +255,64 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     if (s != SK_OK) return s;
     if (!(di.major == 10 && di.minor == 3))
         return fail(SK_ERR_UNSUPPORTED, "this library runs on sm_103 (GB300) only");
-    Plan p;
-    std::string why;
-    s = make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, &o, di.sms, &p, &why);
-    if (s != SK_OK) return fail(s, why);
-    if (p.num_ctas == 0) return SK_OK;  // q_len == 0: nothing to compute
-    const long long total_kv = p.kv_off[size_t(B)];
+    // The plan and the tensor maps depend only on the problem, the options and
+    // the q / k / v / out addresses: a decode loop that repeats a call reuses
+    // them from the per-thread cache instead of planning and encoding again.
+    CallKey key;
+    memset(&key, 0, sizeof key);
+    key.dev = di.dev; key.B = B; key.Hq = Hq; key.Hkv = Hkv; key.q_len = q_len; key.d = d;
+    key.causal = causal ? 1 : 0; key.window_left = window_left < 0 ? -1 : window_left;
+    key.policy = o.policy; key.force_num_splits = o.force_num_splits; key.force_pack_gqa = o.force_pack_gqa;
+    key.force_path = o.force_path; key.max_splits = o.max_splits; key.num_sms = o.num_sms;
+    key.q = q; key.k = k; key.v = v; key.out = out;
+    const CallEntry* ce = kv_len_host ? lookup_call(key, kv_len_host) : nullptr;
+    if (!ce) {
+        CallEntry fresh;
+        std::string why;
+        s = make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, &o, di.sms, &fresh.plan, &why);
+        if (s != SK_OK) return fail(s, why);
+        const Plan& p = fresh.plan;
+        if (p.num_ctas == 0) return SK_OK;  // q_len == 0: nothing to compute
+        const long long total_kv = p.kv_off[size_t(B)];
+        if (!q || !out) return fail(SK_ERR_INVALID_ARG, "NULL q, out, lse or workspace");
+        if (total_kv > 0 && (!k || !v)) return fail(SK_ERR_INVALID_ARG, "NULL k or v");
+        if (!aligned(q, 16) || !aligned(out, 16) || (total_kv > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+            return fail(SK_ERR_MISALIGNED, "q, k, v and out must be 16-byte aligned");
+        if (total_kv >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "at most 2^31 - 1 KV rows in total");
+        // K/V tensor maps.  With no KV rows at all no tile is ever loaded; the
+        // map then points at `out` only so that it is well formed.
+        const void* kb = total_kv > 0 ? k : out;
+        const void* vb = total_kv > 0 ? v : out;
+        const long long rows = total_kv > 0 ? total_kv : 1;
+        if (!make_kv_map(&fresh.tmK, kb, Hkv, d, rows) || !make_kv_map(&fresh.tmV, vb, Hkv, d, rows))
+            return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        // Prefill tiles take Q by TMA when a 128-row half is whole row groups of
+        // the map (128 % gp == 0) and every row index fits the copy's int32
+        // coordinate.  Final prefill outputs (one split per sequence) leave
+        // through the same boxes.
+        memset(&fresh.tmQ, 0, sizeof fresh.tmQ);
+        memset(&fresh.tmO, 0, sizeof fresh.tmO);
+        fresh.q_gp = p.pack_gqa ? p.G : 1;
+        const long long q_rows = (long long)B * q_len;
+        fresh.q_tma = p.path == SK_PATH_PREFILL && 128 % fresh.q_gp == 0 && q_rows < (1LL << 31);
+        if (fresh.q_tma && !make_q_map(&fresh.tmQ, q, q_rows, Hq, d, fresh.q_gp))
+            return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (Q)");
+        fresh.o_tma = fresh.q_tma && !p.needs_combine;
+        if (fresh.o_tma && !make_o_map(&fresh.tmO, out, B, q_len, Hq, d, fresh.q_gp))
+            return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (O)");
+        ce = insert_call(key, std::move(fresh));
+    }
+    const Plan& p = ce->plan;
     if (!q || !out || !lse || !workspace) return fail(SK_ERR_INVALID_ARG, "NULL q, out, lse or workspace");
-    if (total_kv > 0 && (!k || !v)) return fail(SK_ERR_INVALID_ARG, "NULL k or v");
-    if (!aligned(q, 16) || !aligned(out, 16) || (total_kv > 0 && (!aligned(k, 16) || !aligned(v, 16))))
-        return fail(SK_ERR_MISALIGNED, "q, k, v and out must be 16-byte aligned");
     if (!aligned(lse, 4)) return fail(SK_ERR_MISALIGNED, "lse must be 4-byte aligned");
     if (!aligned(workspace, 256)) return fail(SK_ERR_MISALIGNED, "workspace must be 256-byte aligned");
     if (ws_bytes < p.ws_bytes) return fail(SK_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than plan.workspace_bytes");
-    if (total_kv >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "at most 2^31 - 1 KV rows in total");
-
-    // K/V tensor maps.  With no KV rows at all no tile is ever loaded; the map
-    // then points at `out` only so that it is well formed.
-    CUtensorMap tmK, tmV;
-    const void* kb = total_kv > 0 ? k : out;
-    const void* vb = total_kv > 0 ? v : out;
-    const long long rows = total_kv > 0 ? total_kv : 1;
-    if (!make_kv_map(&tmK, kb, Hkv, d, rows) || !make_kv_map(&tmV, vb, Hkv, d, rows))
-        return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    // Prefill tiles take Q by TMA when a 128-row half is whole row groups of the
-    // map (128 % gp == 0) and every row index fits the copy's int32 coordinate.
-    CUtensorMap tmQ;
-    memset(&tmQ, 0, sizeof tmQ);
-    const int q_gp = p.pack_gqa ? p.G : 1;
-    const long long q_rows = (long long)B * q_len;
-    const bool q_tma = p.path == SK_PATH_PREFILL && 128 % q_gp == 0 && q_rows < (1LL << 31);
-    if (q_tma && !make_q_map(&tmQ, q, q_rows, Hq, d, q_gp))
-        return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (Q)");
-    // Final prefill outputs (one split per sequence) leave through the same boxes.
-    CUtensorMap tmO;
-    memset(&tmO, 0, sizeof tmO);
-    const bool o_tma = q_tma && !p.needs_combine;
-    if (o_tma && !make_o_map(&tmO, out, B, q_len, Hq, d, q_gp))
-        return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (O)");
+    const CUtensorMap& tmK = ce->tmK;
+    const CUtensorMap& tmV = ce->tmV;
+    const CUtensorMap& tmQ = ce->tmQ;
+    const CUtensorMap& tmO = ce->tmO;
+    const bool q_tma = ce->q_tma, o_tma = ce->o_tma;
+    const int q_gp = ce->q_gp;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     FwdParams fp;

@@ -201,13 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // commits track exactly the MMAs it issued.
         const bool leader = elect_one();
         constexpr uint32_t idesc_qk = make_idesc_bf16(128, NP, false, false);
-        constexpr uint32_t idesc_pv = make_idesc_bf16(128, NP, true, false);
+        constexpr uint32_t idesc_pv = make_idesc_bf16(128, NP, true, true);
         // Descriptors built once; per MMA only a constant is added to the
         // start-address field (operands lie below 256 KB: no carry).
         const uint64_t kdesc0 = make_sdesc_sw128(stage_k(0), 16, 1024);
         const uint64_t vdesc0 = make_sdesc_sw128(stage_v(0), 16384, 1024);
         const uint64_t qdesc0 = make_sdesc_sw128(sQ, 16, 1024);
-        const uint64_t pdesc0 = make_sdesc_sw128(sP, 16, 1024);
+        // P^T: MN-major, no swizzle; core matrices of 8 keys x 8 rows, rows
+        // adjacent (128 B apart), key groups (NP / 8) * 128 B apart.
+        const uint64_t pdesc0 = make_sdesc_noswz(sP, (NP / 8) * 128, 128);
         bool ok = true;
         if (p.inject_stall) {
             // The injected stall gives up first (half the limit), so the status
@@ -221,14 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
             const int s = jj % ST;
             good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull) && good;
+            // The block that holds the end of the sequence also holds rows of
+            // the next sequence: their P is 0, but 0 * (Inf or NaN) is NaN, so
+            // those V rows are zeroed before the PV MMA reads the slot.
+            const int tail_row = sk - (br.lo + jj) * 128;
+            if (good && tail_row < 128) zero_rows<HD>(stage_v(s), tail_row, lane);
             tc_fence_after();
             __syncwarp();
             if (leader && good) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t a = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
-                    const uint64_t bd =
-                        pdesc0 + uint64_t(((jj & 1) * C::kPBuf + (kk >> 2) * (NP * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = pdesc0 + uint64_t(((jj & 1) * C::kPBuf + kk * 2 * (NP / 8) * 128) >> 4);
                     umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(bar_odone(jj & 1));
@@ -313,112 +319,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_causal = p.causal != 0;
         const bool has_window = p.window_left >= 0;
 
+        // Per row q (identical in every thread): neg_m[q] = -(running max) in
+        // log2 units; +inf while the row has no visible key yet (any visible
+        // score then exceeds the threshold and sets the max); -inf for padding
+        // rows, whose scores thereby become -inf and their P 0.  The running max
+        // itself lives in sm_m and is only read on the rare blocks that raise it.
         float l_t[NP];
+        float neg_m[NP];
 #pragma unroll
-        for (int q = 0; q < NP; ++q) l_t[q] = 0.f;
-        // Running row maxima, identical in every thread (the shared copy sm_m is
-        // only read back after a block raised them).
-        float m_reg[NP];
-#pragma unroll
-        for (int q = 0; q < NP; ++q) m_reg[q] = -INFINITY;
+        for (int q = 0; q < NP; ++q) {
+            l_t[q] = 0.f;
+            neg_m[q] = (q < rows_valid) ? INFINITY : -INFINITY;
+        }
         const float sl2 = p.scale_log2;
-        __nv_bfloat16* const p_smem = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP);
+        const uint32_t p_st = sP + uint32_t((kt >> 3) * (NP / 8) * 128 + (kt & 7) * 16);
+        auto masked = [&](int key, int q) {
+            const int dg = sm_diag[q];
+            return key >= sk || (has_causal && key > dg) || (has_window && key < dg - p.window_left);
+        };
 
         for (int j = 0; j < nblocks; ++j) {
             const int n = br.lo + j;
-            float x[NP];
+            const uint32_t tS = tS0 + (j & 1) * NP + lane_off;
+            float t[NP];  // scaled scores minus the running max, log2 units
             mbar_wait(bar_sfull(j & 1), (j >> 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxSFull);
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < NP / 16; ++c) tmem_ld16(tS0 + (j & 1) * NP + lane_off + c * 16, x + c * 16);
+            for (int c = 0; c < NP / 16; ++c) tmem_ld16(tS + c * 16, t + c * 16);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar_sempty(j & 1));
 
             const int key = n * 128 + kt;
             const int blk_first = n * 128, blk_last = n * 128 + 127;
             const bool need_mask = (blk_last >= sk) || (has_causal && blk_last > diag_lo) ||
                                    (has_window && blk_first < diag_hi - p.window_left);
-            // Scale, then the masks as separate warp-uniform passes: padding rows
-            // only when the tile has them, keys only on boundary blocks.
 #pragma unroll
-            for (int q = 0; q < NP; ++q) x[q] *= sl2;
-            if (rows_valid < NP) {
-#pragma unroll
-                for (int q = 0; q < NP; ++q)
-                    if (q >= rows_valid) x[q] = -INFINITY;
-            }
+            for (int q = 0; q < NP; ++q) t[q] = fmaf(t[q], sl2, neg_m[q]);
             if (need_mask) {
 #pragma unroll
-                for (int q = 0; q < NP; ++q) {
-                    const int dg = sm_diag[q];
-                    if (key >= sk || (has_causal && key > dg) || (has_window && key < dg - p.window_left))
-                        x[q] = -INFINITY;
-                }
+                for (int q = 0; q < NP; ++q)
+                    if (masked(key, q)) t[q] = -INFINITY;
             }
             bool need = false;
 #pragma unroll
-            for (int q = 0; q < NP; ++q) need |= x[q] > m_reg[q] + kRescaleThreshold;
-            const bool need_all = named_bar_or(1, 128, need);
-            if (need_all) {
+            for (int q = 0; q < NP; ++q) need |= t[q] > kRescaleThreshold;
+            if (named_bar_or(1, 128, need)) {
+                // A row's max grew by more than 2^8 (or its first visible key
+                // arrived): reload the raw scores, take every row's block max,
+                // move the running maxima and recompute the scores.  The S buffer
+                // is only released after this, so the reload reads this block.
+#pragma unroll
+                for (int c = 0; c < NP / 16; ++c) tmem_ld16(tS + c * 16, t + c * 16);
+                tmem_wait_ld();
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
-                    const float v = warp_max(x[q]);
+                    float v = t[q] * sl2;
+                    if (need_mask && masked(key, q)) v = -INFINITY;
+                    v = warp_max(v);
                     if (lane == 0) red[(warp & 3) * NP + q] = v;
                 }
                 named_bar_sync(1, 128);
                 if (sidx < NP) {
                     const int q = sidx;
-                    const float bm = fmaxf(fmaxf(red[q], red[NP + q]), fmaxf(red[2 * NP + q], red[3 * NP + q]));
-                    const float mo = sm_m[q];
-                    const float mn = fmaxf(mo, bm);
-                    sm_alpha[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
-                    sm_m[q] = mn;
+                    float a = 1.f;
+                    if (q < rows_valid) {
+                        const float bm = fmaxf(fmaxf(red[q], red[NP + q]), fmaxf(red[2 * NP + q], red[3 * NP + q]));
+                        const float mo = sm_m[q];
+                        const float mn = fmaxf(mo, bm);
+                        a = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);  // l and O are 0 while mo = -inf
+                        sm_m[q] = mn;
+                    }
+                    sm_alpha[q] = a;
                 }
                 named_bar_sync(1, 128);
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
+                    if (q < rows_valid) {
+                        const float mq = sm_m[q];
+                        neg_m[q] = (mq == -INFINITY) ? INFINITY : -mq;
+                    }
                     l_t[q] *= sm_alpha[q];
-                    m_reg[q] = sm_m[q];
+                    t[q] = fmaf(t[q], sl2, neg_m[q]);
+                }
+                if (need_mask) {
+#pragma unroll
+                    for (int q = 0; q < NP; ++q)
+                        if (masked(key, q)) t[q] = -INFINITY;
+                }
+                // Rescaling O needs the previous block's PV to be complete.
+                if (j >= 1) {
+                    mbar_wait(bar_odone((j - 1) & 1), ((j - 1) >> 1) & 1, wc,
+                              (kKernDecode << 8) | kSiteSoftmaxODone);
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < NP / 16; ++c) {
+                        float o[16];
+                        tmem_ld16(tO + lane_off + c * 16, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
+                        tmem_st16(tO + lane_off + c * 16, o);
+                    }
+                    tmem_wait_st();
                 }
             }
+            tc_fence_before();
+            mbar_arrive(bar_sempty(j & 1));
+
+            // P = 2^t, summed per row, packed as bf16 pairs of consecutive rows.
+            uint32_t pk[NP / 2];
 #pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                const float mq = m_reg[q];
-                const float pv = (mq == -INFINITY) ? 0.f : fast_exp2(x[q] - mq);
-                l_t[q] += pv;
-                x[q] = pv;
-            }
-            // Rescaling O needs the previous block's PV to be complete.
-            if (need_all && j >= 1) {
-                mbar_wait(bar_odone((j - 1) & 1), ((j - 1) >> 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < NP / 16; ++c) {
-                    float o[16];
-                    tmem_ld16(tO + lane_off + c * 16, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] *= sm_alpha[c * 16 + e];
-                    tmem_st16(tO + lane_off + c * 16, o);
-                }
-                tmem_wait_st();
+            for (int e = 0; e < NP / 2; ++e) {
+                const float p0 = fast_exp2(t[2 * e]);
+                const float p1 = fast_exp2(t[2 * e + 1]);
+                l_t[2 * e] += p0;
+                l_t[2 * e + 1] += p1;
+                pk[e] = pack_bf16x2(p0, p1);
             }
             // P buffer (j & 1) was last read by the PV of block j - 2.
             if (j >= 2) {
                 mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
-            // P^T[q][kt] (bf16) -> smem, K-major over keys, 128B swizzle.  Plain
-            // stores, so the compiler may schedule them; the proxy fence below
-            // orders them before the MMA reads the buffer.
+            // P^T -> smem, MN-major without swizzle: key kt's 8 consecutive rows
+            // form one 16-byte line of a core matrix ([key / 8][row / 8][key % 8][row % 8]).
             {
-                const uint32_t base = uint32_t((j & 1) * C::kPBuf + (kt >> 6) * (NP * 128));
-                const int g = (kt & 63) >> 3;
-                const uint32_t within = (kt & 7) * 2;
+                const uint32_t dst = p_st + uint32_t((j & 1) * C::kPBuf);
 #pragma unroll
-                for (int q = 0; q < NP; ++q)
-                    p_smem[(base + sw128_offset(q, g) + within) >> 1] = __float2bfloat16_rn(x[q]);
+                for (int g = 0; g < NP / 8; ++g)
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + g * 128), "r"(pk[4 * g]),
+                                 "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                                 : "memory");
             }
             fence_proxy_async_smem();
             tc_fence_before();

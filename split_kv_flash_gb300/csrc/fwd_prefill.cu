@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(bar_never, 0, wc_half, (kKernPrefill << 8) | kSiteInjected);
         }
         auto active = [&](int t, int j) { return j >= first[t] && j < first[t] + count[t]; };
+        int zeroed_step = -1;  // visiting step whose V tail rows were zeroed
         // O_t += P_t . V(j), the i-th block of half t.  P_t sits in the upper
         // columns of S_t; the QK^T that next overwrites S_t is issued after
         // this MMA, and the tensor pipe runs a CTA's MMAs in issue order.
@@ -246,6 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = j % VST;
             bool good = mbar_wait(bar_pfull(t), i & 1, wc, (kKernPrefill << 8) | kSiteMmaPFull);
             good = mbar_wait(bar_vfull(s), (j / VST) & 1, wc, (kKernPrefill << 8) | kSiteMmaFull) && good;
+            // The block that holds the end of the sequence also holds rows of
+            // the next sequence: their P is 0, but 0 * (Inf or NaN) is NaN, so
+            // those V rows are zeroed before the first PV MMA reads the slot.
+            const int tail_row = sk - (br.hi - 1 - j) * 128;
+            if (good && tail_row < 128 && zeroed_step != j) zero_rows<HD>(stage_v(s), tail_row, lane);
+            zeroed_step = j;
             tc_fence_after();
             __syncwarp();
             if (leader) {

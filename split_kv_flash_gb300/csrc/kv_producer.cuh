@@ -69,6 +69,22 @@ __device__ __forceinline__ bool produce_kv_tile(const CUtensorMap* tmK, const CU
     return true;
 }
 
+// Zero rows [first, 128) of a 128-row K/V block in shared memory (HD / 64
+// chunks of 128 rows x 128 bytes; a whole row is zeroed, so its swizzle does
+// not matter), by the 32 lanes of one warp, then make the zeros visible to the
+// tensor cores (async proxy).  Called after the block's copy has completed.
+template <int HD>
+__device__ __forceinline__ void zero_rows(uint32_t slot, int first, int lane) {
+    const int n16 = (128 - first) * 8;  // 16-byte granules per chunk
+#pragma unroll
+    for (int c = 0; c < HD / 64; ++c)
+        for (int idx = lane; idx < n16; idx += 32)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(slot + c * 16384 + first * 128 + idx * 16),
+                         "r"(0u)
+                         : "memory");
+    fence_proxy_async_smem();
+}
+
 // Before the CTA exits: the last load of every slot (ring positions below
 // `loaded`) must have landed.
 __device__ __forceinline__ void drain_ring(const KvRing& R, int loaded, uint64_t limit_ns) {

@@ -301,6 +301,20 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// Shared-memory matrix descriptor for an operand without swizzle, built from
+// 8 x 16-byte core matrices (128 contiguous bytes each).  For an MN-major
+// operand a core matrix holds 8 K-rows of 8 consecutive M/N elements;
+// `lbo` is the byte distance between core matrices adjacent along K, `sbo`
+// between core matrices adjacent along M/N.  [61,64) layout 0 = no swizzle.
+__device__ __forceinline__ uint64_t make_sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+    d |= uint64_t(1) << 46;
+    return d;
+}
+
 // Byte offset, inside a K-major SW128 tile stored as [K/64 chunks][rows][128 B],
 // of the 16-byte granule (row, granule g in 0..7) -- the TMA SWIZZLE_128B pattern.
 __device__ __forceinline__ uint32_t sw128_offset(int row, int g) {

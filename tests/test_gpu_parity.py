@@ -25,10 +25,14 @@ def _check_full(sk, w, opts=None, tag=None):
     return H.compare_full(out, lse, ref_o, ref_l, tag or w.name)
 
 
-def _check_sampled(sk, w, n_rows, opts=None):
+def _check_sampled(sk, w, n_rows, opts=None, full_heads=None):
+    """Sampled rows, plus every query row of the (b, h) heads in full_heads."""
     q, k, v = wl.make_inputs(w)
     out, lse = H.run_gpu(sk, w, q, k, v, opts)
     rows = H.sample_rows(w, n_rows)
+    if full_heads:
+        extra = np.array([(b, h, i) for b, h in full_heads for i in range(w.q_len)], dtype=np.int32)
+        rows = np.unique(np.concatenate([rows, extra]), axis=0)
     ref_o, ref_l = oracle.attn_rows(wl.bits(q), wl.bits(k), wl.bits(v), w.kv_len, w.scale, rows,
                                     w.causal, w.window_left)
     return H.compare_rows(out, lse, rows, ref_o, ref_l, w.name)
@@ -58,12 +62,15 @@ def test_varlen_decode(sk, B):
 
 @pytest.mark.parametrize("B", [16, 32])
 def test_varlen_decode_large(sk, B):
-    _check_sampled(sk, wl.varlen_decode(B), 192)
+    _check_full(sk, wl.varlen_decode(B))
 
 
 @pytest.mark.parametrize("local", [False, True])
 def test_prefill_8192(sk, local):
-    _check_sampled(sk, wl.prefill(local), 384)
+    """Sampled rows over every head, plus one whole head of every sequence: all
+    32 m blocks of it, both 128-row halves of each, every LPT launch position."""
+    w = wl.prefill(local)
+    _check_sampled(sk, w, 384, full_heads=[(b, (7 * b + 3) % w.Hq) for b in range(w.B)])
 
 
 # ----------------------------------------------------------- shapes and edges
@@ -139,3 +146,42 @@ def test_decode_forced_onto_prefill_kernel(sk):
     opts = sk.Opts()
     opts.force_path = sk.SK_PATH_PREFILL
     _check_full(sk, w, opts, "gqa_decode_on_prefill_kernel")
+
+
+# ------------------------------------------------ rows outside a sequence
+
+NEIGHBOUR = [
+    # name, B, Hq, Hkv, q_len, kv_len, causal
+    ("decode_varlen", 3, 8, 2, 1, [300, 200, 129], False),
+    ("verify_uniform", 2, 4, 4, 9, [300, 300], True),
+    ("prefill_uniform", 2, 4, 2, 300, [300, 300], True),
+]
+
+
+@pytest.mark.parametrize("case", NEIGHBOUR, ids=[c[0] for c in NEIGHBOUR])
+def test_rows_past_a_sequence_never_leak(sk, case):
+    """The 128-row block holding the end of a sequence also holds the first
+    rows of the next one.  Here those rows carry +Inf, -Inf and NaN in K and V;
+    every sequence whose own keys are finite must still match the oracle."""
+    name, B, Hq, Hkv, sq, kv, causal = case
+    w = wl.Workload(name, B, Hq, Hkv, 128, sq, kv, causal=causal, seed=31)
+    q, k, v = wl.make_inputs(w)
+    off = np.concatenate([[0], np.cumsum(kv)])
+    bad = {1}  # sequence 1's first rows are poisoned; its own result is not checked
+    r0 = int(off[1])
+    k[r0:r0 + 3] = float("nan")
+    k[r0 + 3:r0 + 6] = float("inf")
+    v[r0:r0 + 3] = float("inf")
+    v[r0 + 3:r0 + 6] = float("nan")
+    v[r0 + 6:r0 + 9] = -float("inf")
+    out, lse = H.run_gpu(sk, w, q, k, v)
+    for b in range(B):
+        if b in bad:
+            continue
+        wb = wl.Workload(name, 1, Hq, Hkv, 128, sq, [kv[b]], causal=causal)
+        qb = q[b:b + 1]
+        kb = k[int(off[b]):int(off[b + 1])]
+        vb = v[int(off[b]):int(off[b + 1])]
+        ref_o, ref_l = oracle.attn_fwd(wl.bits(qb), wl.bits(kb), wl.bits(vb), wb.kv_len, wb.scale,
+                                       wb.causal, wb.window_left)
+        H.compare_full(out[b:b + 1], lse[b:b + 1], ref_o, ref_l, "%s_seq%d" % (name, b))

@@ -59,7 +59,38 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep")
+    ap.add_argument("--workload", default=None,
+                    help="profiling helper: run --steps calls of one named workload and exit "
+                         "(names: see --list-workloads)")
+    ap.add_argument("--list-workloads", action="store_true")
     return ap.parse_args()
+
+
+def named_workloads():
+    """Every workload by its short name (the sweep's, the headline and prefill)."""
+    ws = {short_name(w.name): w for w in sweep_workloads()}
+    ws["gqa_kv131072"] = wl.gqa_decode(131072)
+    ws["prefill_causal"] = wl.prefill(False)
+    ws["prefill_local1024"] = wl.prefill(True)
+    return ws
+
+
+def run_named(sk, name, calls, device):
+    """Profiling helper: `calls` back-to-back calls of one workload on inputs
+    drawn on the device; checks the device status word at the end."""
+    w = named_workloads()[name]
+    g = torch.Generator(device=device).manual_seed(w.seed)
+    q = torch.randn((w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
+    k = (torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g) * w.k_scale).to(torch.bfloat16)
+    v = torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g).to(torch.bfloat16)
+    out, lse, ws = sk.attn_fwd(q, k, v, w.kv_len, w.scale, w.causal, w.window_left)
+    for _ in range(calls):
+        sk.attn_fwd(q, k, v, w.kv_len, w.scale, w.causal, w.window_left, out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize(device)
+    st, where = sk.sk_attn_workspace_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d at %d" % (st, where))
+    print(json.dumps({"workload": w.name, "calls": calls + 1, "status": "ok"}), flush=True)
 
 
 # --------------------------------------------------------------------- env
@@ -598,6 +629,9 @@ def main():
     global _pg
     args = parse()
     world, rank, local = dist_env()
+    if args.list_workloads:
+        print("\n".join(sorted(named_workloads())))
+        return
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
@@ -616,6 +650,10 @@ def main():
     sk.lib()
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+    if args.workload:
+        if rank == 0:
+            run_named(sk, args.workload, args.steps, device)
+        return
     if args.no_decode:  # profiling helper: the prefill kernels alone
         pre = {}
         for local_w in (False, True):

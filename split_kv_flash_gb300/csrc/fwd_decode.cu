@@ -36,10 +36,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+// Maximum over the 32 lanes of a converged warp, one instruction
+// (redux.sync on f32; NaN inputs are not expected here).
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -49,17 +51,19 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <int HD, int NP>
 struct DecodeCfg {
-    static constexpr int kStages = HD == 128 ? (NP <= 32 ? 3 : 2) : (NP <= 32 ? 4 : 3);
+    // Ring depths: the next QK^T waits on a K block, so K gets the deeper ring;
+    // V has a softmax pass of slack.  Each (HD, NP) takes what shared memory allows.
+    static constexpr int kStagesK = HD == 128 ? 3 : 4;
+    static constexpr int kStagesV = HD == 128 ? (NP <= 32 ? 3 : 2) : (NP <= 32 ? 4 : 3);
     static constexpr int kKBytes = 128 * HD * 2;      // K block: 128 rows x HD
     static constexpr int kVBytes = 128 * 128 * 2;     // V block region: 128 rows x 128 (M = 128 for PV)
     static constexpr int kVLoadBytes = 128 * HD * 2;  // bytes actually loaded
-    static constexpr int kStageBytes = kKBytes + kVBytes;  // one K slot + one V slot
     static constexpr int kQBytes = NP * HD * 2;
     static constexpr int kPBuf = NP * 128 * 2;             // one P^T buffer
     static constexpr int kPBytes = 2 * kPBuf;                // double-buffered
-    static constexpr int kOffK = 0;                        // K ring: kStages slots
-    static constexpr int kOffV = kStages * kKBytes;        // V ring: kStages slots
-    static constexpr int kOffQ = kStages * kStageBytes;
+    static constexpr int kOffK = 0;                        // K ring: kStagesK slots
+    static constexpr int kOffV = kStagesK * kKBytes;       // V ring: kStagesV slots
+    static constexpr int kOffQ = kOffV + kStagesV * kVBytes;
     static constexpr int kOffP = kOffQ + kQBytes;
     static constexpr int kOffRed = kOffP + kPBytes;            // float red[4][NP]
     static constexpr int kOffM = kOffRed + 4 * NP * 4;         // float m[NP]
@@ -67,7 +71,7 @@ struct DecodeCfg {
     static constexpr int kOffL = kOffAlpha + NP * 4;           // float l[NP]
     static constexpr int kOffDiag = kOffL + NP * 4;            // int diag[NP]
     static constexpr int kOffBars = (kOffDiag + NP * 4 + 7) / 8 * 8;
-    static constexpr int kNumBars = 4 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+    static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 1 + 1;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;   // tmem base, abort flag
     static constexpr int kSmemBytes = kOffMisc + 16;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1024
@@ -82,7 +86,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_decode_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Seqs seqs) {
     using C = DecodeCfg<HD, NP>;
-    constexpr int ST = C::kStages;
+    constexpr int KST = C::kStagesK;
+    constexpr int VST = C::kStagesV;
+    constexpr int NB0 = 2 * KST + 2 * VST;  // first barrier after the rings
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -125,27 +131,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sm_l = reinterpret_cast<float*>(smem + C::kOffL);
     int* sm_diag = reinterpret_cast<int*>(smem + C::kOffDiag);
     const uint32_t bars = sbase + C::kOffBars;
-    // barriers: kfull[ST] kempty[ST] vfull[ST] vempty[ST] sfull[2] sempty[2] pfull[2] odone[2] q never drain
+    // barriers: kfull[KST] kempty[KST] vfull[VST] vempty[VST] sfull[2] sempty[2] pfull[2] odone[2] q never drain
     auto bar_kfull = [&](int s) { return bars + 8u * s; };
-    auto bar_kempty = [&](int s) { return bars + 8u * (ST + s); };
-    auto bar_vfull = [&](int s) { return bars + 8u * (2 * ST + s); };
-    auto bar_vempty = [&](int s) { return bars + 8u * (3 * ST + s); };
-    auto bar_sfull = [&](int i) { return bars + 8u * (4 * ST + i); };
-    auto bar_sempty = [&](int i) { return bars + 8u * (4 * ST + 2 + i); };
-    auto bar_pfull = [&](int i) { return bars + 8u * (4 * ST + 4 + i); };
-    auto bar_odone = [&](int i) { return bars + 8u * (4 * ST + 6 + i); };
-    const uint32_t bar_qfull = bars + 8u * (4 * ST + 8);
-    const uint32_t bar_never = bars + 8u * (4 * ST + 9);
-    const uint32_t bar_drain = bars + 8u * (4 * ST + 10);
+    auto bar_kempty = [&](int s) { return bars + 8u * (KST + s); };
+    auto bar_vfull = [&](int s) { return bars + 8u * (2 * KST + s); };
+    auto bar_vempty = [&](int s) { return bars + 8u * (2 * KST + VST + s); };
+    auto bar_sfull = [&](int i) { return bars + 8u * (NB0 + i); };
+    auto bar_sempty = [&](int i) { return bars + 8u * (NB0 + 2 + i); };
+    auto bar_pfull = [&](int i) { return bars + 8u * (NB0 + 4 + i); };
+    auto bar_odone = [&](int i) { return bars + 8u * (NB0 + 6 + i); };
+    const uint32_t bar_qfull = bars + 8u * (NB0 + 8);
+    const uint32_t bar_never = bars + 8u * (NB0 + 9);
+    const uint32_t bar_drain = bars + 8u * (NB0 + 10);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
     auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(bar_kfull(s), 1);
             mbar_init(bar_kempty(s), 1);
+        }
+        for (int s = 0; s < VST; ++s) {
             mbar_init(bar_vfull(s), 1);
             mbar_init(bar_vempty(s), 1);
         }
@@ -189,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ===================== TMA producer (K and V rings): the whole warp
         // runs the loop, one elected lane issues the copies.
         const bool leader = elect_one();
-        const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), ST};
-        const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), ST};
+        const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
+        const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
         const int kvh = p.pack_gqa ? ht : ht / p.G;
         produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, false, l2_policy_evict_first(), wc,
                        (kKernDecode << 8) | kSiteProducerEmpty, leader);
@@ -221,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(bar_qfull, 0, wc, (kKernDecode << 8) | kSiteMmaQ) && ok;
         auto issue_pv = [&](int jj) {
             bool good = mbar_wait(bar_pfull(jj & 1), (jj >> 1) & 1, wc, (kKernDecode << 8) | kSiteMmaPFull);
-            const int s = jj % ST;
-            good = mbar_wait(bar_vfull(s), (jj / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull) && good;
+            const int s = jj % VST;
+            good = mbar_wait(bar_vfull(s), (jj / VST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull) && good;
             // The block that holds the end of the sequence also holds rows of
             // the next sequence: their P is 0, but 0 * (Inf or NaN) is NaN, so
             // those V rows are zeroed before the PV MMA reads the slot.
@@ -242,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         for (int j = 0; j < nblocks; ++j) {
-            const int s = j % ST;
-            bool good = mbar_wait(bar_kfull(s), (j / ST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
+            const int s = j % KST;
+            bool good = mbar_wait(bar_kfull(s), (j / KST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
             if (j >= 2)
                 good = mbar_wait(bar_sempty(j & 1), ((j >> 1) - 1) & 1, wc,
                                  (kKernDecode << 8) | kSiteMmaSEmpty) && good;
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < NP; ++q) {
                     float v = t[q] * sl2;
                     if (need_mask && masked(key, q)) v = -INFINITY;
-                    v = warp_max(v);
+                    v = warp_max_f32(v);
                     if (lane == 0) red[(warp & 3) * NP + q] = v;
                 }
                 named_bar_sync(1, 128);

@@ -75,6 +75,17 @@ typedef enum {
     SK_PATH_PREFILL = 2   /* 256-row tiles: two 128-row halves that share each K/V block; query rows on the MMA M axis */
 } sk_path;
 
+/* How the split partials are merged (sk_attn_opts.combine_mode; the stream-k
+ * fixup of the llama.cpp PR #21086 review, the combine step of the tiling
+ * chapter section 5.1). */
+typedef enum {
+    SK_COMBINE_AUTO = 0,      /* the library chooses (SK_COMBINE_IN_KERNEL where it applies) */
+    SK_COMBINE_KERNEL = 1,    /* a second kernel merges every split row */
+    SK_COMBINE_IN_KERNEL = 2  /* one launch: the last split CTA of a tile to finish merges the
+                                 tile's partials (decode path, when they fit its shared memory;
+                                 otherwise the second kernel is used) */
+} sk_combine_mode;
+
 /* Options; an all-zero struct (or NULL) selects the defaults. */
 typedef struct {
     int policy;            /* sk_split_policy */
@@ -89,6 +100,7 @@ typedef struct {
                               timeout path; the kernel reports SK_ERR_DEVICE_TIMEOUT) */
     void* event_begin;     /* optional cudaEvent_t recorded just before the partial kernel */
     void* event_end;       /* optional cudaEvent_t recorded just after it */
+    int combine_mode;      /* sk_combine_mode */
 } sk_attn_opts;
 
 /* The host scheduler's decisions for one problem. */
@@ -110,6 +122,8 @@ typedef struct {
     size_t echo_offset;       /* byte offset of the plan echo in the workspace */
     size_t lse_part_offset;   /* byte offset of LSE partials [S][B][Hq][q_len] fp32 */
     size_t o_part_offset;     /* byte offset of O partials [S][B][Hq][q_len][d] fp32 */
+    int combine_in_kernel;    /* 1: the partial kernel merges the splits itself (no second launch) */
+    size_t counter_offset;    /* byte offset of the per-tile arrival counters [tiles] uint32 */
 } sk_attn_plan_info;
 
 /* Plan only (host, no device work).  Fills *info.  Same argument meaning as
@@ -132,7 +146,9 @@ sk_status sk_attn_plan_ranges(int B, int Hq, int Hkv, int q_len, const int* kv_l
  * 256-byte aligned, zero-filled once before its first use (every call leaves its
  * status word at zero unless a kernel timed out); it may be reused by consecutive
  * calls on the same stream, but calls that overlap on the GPU need separate
- * workspaces.  Returns SK_OK once the kernels are enqueued. */
+ * workspaces.  After a call that reported SK_ERR_DEVICE_TIMEOUT the workspace
+ * must be zero-filled again before its next use.  Returns SK_OK once the
+ * kernels are enqueued. */
 sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                       int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d,
                       float scale, int causal, int window_left,

@@ -16,7 +16,7 @@ __all__ = [
     "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_status_string",
     "sk_attn_fwd_noalloc", "sk_attn_noalloc_status", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
-    "SK_PATH_PREFILL", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
+    "SK_PATH_PREFILL", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
 ]
 
@@ -28,6 +28,7 @@ SK_ERR_MISALIGNED, SK_ERR_CUDA, SK_ERR_DEVICE_TIMEOUT = 4, 5, 6
 SK_POLICY_DEFAULT, SK_POLICY_FILL, SK_POLICY_FA_HEURISTIC = 0, 1, 2
 SK_POLICY_FIXED_CHUNK, SK_POLICY_MIN_CHUNK = 3, 4
 SK_PATH_AUTO, SK_PATH_DECODE, SK_PATH_PREFILL = 0, 1, 2
+SK_COMBINE_AUTO, SK_COMBINE_KERNEL, SK_COMBINE_IN_KERNEL = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 16 << 20  # SK_NOALLOC_SCRATCH_BYTES in include/sk_attn.h
 
 
@@ -39,6 +40,7 @@ class Opts(ctypes.Structure):
         ("debug_echo_plan", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
         ("debug_inject_stall", ctypes.c_int),
         ("event_begin", ctypes.c_void_p), ("event_end", ctypes.c_void_p),
+        ("combine_mode", ctypes.c_int),
     ]
 
 
@@ -52,7 +54,8 @@ class PlanInfo(ctypes.Structure):
         ("grid_z", ctypes.c_int), ("num_ctas", ctypes.c_longlong),
         ("needs_combine", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("echo_offset", ctypes.c_size_t), ("lse_part_offset", ctypes.c_size_t),
-        ("o_part_offset", ctypes.c_size_t),
+        ("o_part_offset", ctypes.c_size_t), ("combine_in_kernel", ctypes.c_int),
+        ("counter_offset", ctypes.c_size_t),
     ]
 
     def as_dict(self):

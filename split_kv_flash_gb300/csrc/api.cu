@@ -127,7 +127,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ---- per-thread cache of plans and tensor maps
 struct CallKey {
     int dev, B, Hq, Hkv, q_len, d, causal, window_left;
-    int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms;
+    int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms, combine_mode, unused;
     const void *q, *k, *v, *out;
 };
 
@@ -264,6 +264,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     key.causal = causal ? 1 : 0; key.window_left = window_left < 0 ? -1 : window_left;
     key.policy = o.policy; key.force_num_splits = o.force_num_splits; key.force_pack_gqa = o.force_pack_gqa;
     key.force_path = o.force_path; key.max_splits = o.max_splits; key.num_sms = o.num_sms;
+    key.combine_mode = o.combine_mode;
     key.q = q; key.k = k; key.v = v; key.out = out;
     const CallEntry* ce = kv_len_host ? lookup_call(key, kv_len_host) : nullptr;
     if (!ce) {
@@ -323,6 +324,8 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     fp.o_part = reinterpret_cast<float*>(ws + p.o_off);
     fp.lse_part = reinterpret_cast<float*>(ws + p.lse_off);
     fp.echo = reinterpret_cast<int32_t*>(ws + p.echo_off);
+    fp.counters = reinterpret_cast<uint32_t*>(ws + p.cnt_off);
+    fp.fused_combine = p.fused_combine ? 1 : 0;
 
     fp.status = reinterpret_cast<uint32_t*>(ws);
     fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.G = p.G; fp.sq = q_len; fp.d = d;
@@ -351,7 +354,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     if (e != cudaSuccess) return fail_cuda(e, "partial kernel launch");
     if (o.event_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_end), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
-    if (p.needs_combine) {
+    if (p.needs_combine && !p.fused_combine) {
         e = launch_combine(p, fp, stream);
         if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
     }
@@ -399,6 +402,6 @@ const char* sk_attn_status_string(sk_status s) {
 
 const char* sk_attn_last_error(void) { return g_last_error.c_str(); }
 
-int sk_attn_version(void) { return 100; }
+int sk_attn_version(void) { return 101; }
 
 }  // extern "C"

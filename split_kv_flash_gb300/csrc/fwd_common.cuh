@@ -24,6 +24,7 @@ enum : uint32_t {
     kSiteSoftmaxODone = 7,
     kSiteInjected = 8,
     kSiteSmemAlign = 9,
+    kSiteMerge = 10,
 };
 
 struct FwdParams {
@@ -33,6 +34,7 @@ struct FwdParams {
     float* o_part;     // [S][B][Hq][sq][d]
     float* lse_part;   // [S][B][Hq][sq]
     int32_t* echo;     // 4 int32 per CTA
+    uint32_t* counters;  // per tile: split CTAs that have written their partial (in-kernel merge)
     uint32_t* status;  // workspace header word
     int B, Hq, Hkv, G, sq, d;
     int pack_gqa;
@@ -49,6 +51,7 @@ struct FwdParams {
     int q_tma;         // prefill: Q halves arrive by TMA through the 4-D Q map
     int q_gp;          // query heads per row group of that map (G with PackGQA, else 1)
     int o_tma;         // prefill: final O halves leave by TMA through the 5-D O map
+    int fused_combine; // decode: the last split CTA of a tile merges the tile's partials
 };
 
 // Per-sequence lengths, offsets and split counts.  Equal lengths need no table.

@@ -13,10 +13,10 @@
 // normalised partial O and log-sum-exp for the combine kernel, or the final
 // output when the sequence has a single split.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads of K/V blocks into a
-// multi-stage shared-memory ring; warp 1 owns TMEM and issues the MMAs; warps
-// 2-5 (128 threads, thread t <-> TMEM lane t = key t of S^T and d-row t of O^T)
-// do the softmax, the rescaling and the epilogue.
+// Warp roles (224 threads): warps 0 and 6 issue the TMA loads of K and of V
+// blocks into two multi-stage shared-memory rings; warp 1 owns TMEM and issues
+// the MMAs; warps 2-5 (128 threads, thread t <-> TMEM lane t = key t of S^T and
+// d-row t of O^T) do the softmax, the rescaling and the epilogue.
 #include <math.h>
 
 #include "fwd_common.cuh"
@@ -26,7 +26,7 @@
 namespace sk {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -71,8 +71,10 @@ struct DecodeCfg {
     static constexpr int kOffL = kOffAlpha + NP * 4;           // float l[NP]
     static constexpr int kOffDiag = kOffL + NP * 4;            // int diag[NP]
     static constexpr int kOffBars = (kOffDiag + NP * 4 + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 1 + 1;
-    static constexpr int kOffMisc = kOffBars + kNumBars * 8;   // tmem base, abort flag
+    static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 1;
+    static constexpr int kOffMisc = kOffBars + kNumBars * 8;   // tmem base, abort flag, merge flag
+    static constexpr int kRingBytes = kStagesK * kKBytes + kStagesV * kVBytes;
+    static_assert(kRingBytes == decode_ring_bytes(HD, NP), "ring geometry shared with the scheduler");
     static constexpr int kSmemBytes = kOffMisc + 16;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1024
     static constexpr int kTmemCols = (3 * NP <= 32) ? 32 : (3 * NP <= 64) ? 64 : (3 * NP <= 128) ? 128 : 256;
@@ -80,6 +82,99 @@ struct DecodeCfg {
     static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBuf % 1024 == 0 && kOffV % 1024 == 0,
                   "UMMA operands need 1024-byte alignment");
 };
+
+// In-kernel merge of a tile's split partials (the stream-k fixup of the
+// llama.cpp PR #21086 review, done by the partial kernel itself): every split
+// CTA of the tile has written its normalised partial rows (O_s, LSE_s); the
+// last one to arrive on the tile's counter merges them,
+//   LSE = M + ln sum_s exp(LSE_s - M),  O = sum_s exp(LSE_s - LSE) O_s,
+// and writes the final bf16 O and LSE.  The tile's rows of one split are one
+// contiguous run of the partial buffer (heads of the tile x query positions),
+// so each split arrives by one bulk copy into the CTA's free K/V rings while
+// the weights are computed from the LSE partials.  128 threads (the softmax
+// warps); the scheduler only picks this mode when the staged partials fit the
+// rings.  Writers publish with a fence before the counter increment; the
+// merging CTA fences after it and before its bulk copies read the partials.
+template <int HD, int NP>
+__device__ __noinline__ void merge_tile(const FwdParams& p, int b, int ht, int sb, int rows, int sidx, int w4,
+                                        int lane, uint8_t* ring, uint8_t* wbuf_raw, float* lse_row, uint32_t bar,
+                                        volatile int* flag, const WaitCtl& wc) {
+    const int tile = b * p.head_tiles + ht;  // decode tiles have one m block
+    __threadfence();
+    named_bar_sync(1, 128);
+    if (sidx == 0) {
+        const uint32_t prev = atomicAdd(p.counters + tile, 1u);
+        *flag = (prev + 1u == uint32_t(sb)) ? 1 : 0;
+    }
+    named_bar_sync(1, 128);
+    if (!*flag) return;
+    __threadfence();
+    // Rows of the tile in memory order: heads h0 .. h0 + nh - 1, each q_len rows.
+    const int h0 = p.pack_gqa ? ht * p.G : ht;
+    const int nh = p.pack_gqa ? p.G : 1;
+    const size_t stride = size_t(p.B) * p.Hq * p.sq;  // rows between splits
+    const size_t base = (size_t(b) * p.Hq + h0) * p.sq;
+    const uint32_t bytes = uint32_t(rows) * HD * 4u;
+    const uint32_t ring_s = smem_u32(ring);
+    if (sidx == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_expect_tx(bar, bytes * uint32_t(sb));
+        for (int s = 0; s < sb; ++s)
+            bulk_copy_g2s(ring_s + uint32_t(s) * bytes, p.o_part + (size_t(s) * stride + base) * HD, bytes, bar);
+    }
+    // Weights w[r][s] (the P buffers are free) and the merged LSE per row; warp
+    // w4 takes rows w4, w4 + 4, ...; lane t holds splits t, t + 32, ...
+    float* wbuf = reinterpret_cast<float*>(wbuf_raw);
+    constexpr float kLog2e = 1.4426950408889634074f;
+    for (int r = w4; r < rows; r += 4) {
+        const size_t rm = base + size_t(r % nh) * p.sq + r / nh;  // packed row r = i * nh + g
+        float l[kMaxSplits / 32];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < kMaxSplits / 32; ++t) {
+            const int sp = t * 32 + lane;
+            l[t] = sp < sb ? __ldcg(p.lse_part + size_t(sp) * stride + rm) : -INFINITY;
+            mx = fmaxf(mx, l[t]);
+        }
+        mx = warp_max_f32(mx);
+        float sum = 0.f;
+#pragma unroll
+        for (int t = 0; t < kMaxSplits / 32; ++t) sum += (l[t] == -INFINITY) ? 0.f : exp2f((l[t] - mx) * kLog2e);
+        sum = warp_sum(sum);
+        const float lse = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+#pragma unroll
+        for (int t = 0; t < kMaxSplits / 32; ++t) {
+            const int sp = t * 32 + lane;
+            if (sp < sb) wbuf[r * sb + sp] = (l[t] == -INFINITY || lse == -INFINITY) ? 0.f : exp2f((l[t] - lse) * kLog2e);
+        }
+        if (lane == 0) lse_row[r] = lse;
+    }
+    named_bar_sync(1, 128);
+    mbar_wait(bar, 0, wc, (kKernDecode << 8) | kSiteMerge);
+    // O rows: item = (row r, float4 column c); splits summed from shared memory.
+    constexpr int kC4 = HD / 4;
+    for (int it = sidx; it < rows * kC4; it += 128) {
+        const int r = it / kC4, c = it - r * kC4;
+        const int g = r % nh, i = r / nh;
+        const int rmem = g * p.sq + i;  // row in the staged (memory) order
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < sb; ++sp) {
+            const float wgt = wbuf[r * sb + sp];
+            const float4 v = *reinterpret_cast<const float4*>(ring + (size_t(sp) * rows + rmem) * HD * 4 + c * 16);
+            acc.x += wgt * v.x;
+            acc.y += wgt * v.y;
+            acc.z += wgt * v.z;
+            acc.w += wgt * v.w;
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(p.out + ((size_t(b) * p.sq + i) * p.Hq + h0 + g) * HD + c * 4) = packed;
+        if (c == 0) p.lse[(size_t(b) * p.Hq + h0 + g) * p.sq + i] = lse_row[r];
+    }
+    if (sidx == 0) p.counters[tile] = 0u;  // ready for the next call on this workspace
+    mbar_drain(bar, 0, wc.limit_ns);        // no bulk copy may still be writing when the CTA exits
+}
 
 template <int HD, int NP, class Seqs>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -143,8 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_qfull = bars + 8u * (NB0 + 8);
     const uint32_t bar_never = bars + 8u * (NB0 + 9);
     const uint32_t bar_drain = bars + 8u * (NB0 + 10);
+    const uint32_t bar_merge = bars + 8u * (NB0 + 11);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
     auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
     auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
@@ -168,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_qfull, 128);
         mbar_init(bar_never, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_merge, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -193,15 +291,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 2 * NP;   // O^T: columns [2NP, 3NP)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
-    if (warp == 0) {
-        // ===================== TMA producer (K and V rings): the whole warp
-        // runs the loop, one elected lane issues the copies.
+    if (warp == 0 || warp == 6) {
+        // ===================== TMA producers: warp 0 streams K, warp 6 streams V,
+        // each into its own ring (whole warp runs the loop, one elected lane
+        // issues the copies).
         const bool leader = elect_one();
-        const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
-        const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
         const int kvh = p.pack_gqa ? ht : ht / p.G;
-        produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, false, l2_policy_evict_first(), wc,
-                       (kKernDecode << 8) | kSiteProducerEmpty, leader);
+        const KvRing ring = warp == 0 ? KvRing{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST}
+                                      : KvRing{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
+        produce_ring<HD>(warp == 0 ? &tmK : &tmV, ring, nblocks, kvh * HD, kv_off + br.lo * 128, false,
+                         l2_policy_evict_first(), wc, (kKernDecode << 8) | kSiteProducerEmpty, leader);
     } else if (warp == 1) {
         // ===================== MMA issuer
         // The whole warp runs the schedule (warp-uniform control flow and
@@ -275,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (leader) umma_commit(bar_drain);
         mbar_drain(bar_drain, 0, p.timeout_ns);
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ===================== softmax / correction / epilogue (128 threads)
         const int sidx = threadIdx.x - 64;            // 0..127 for cooperative loops
         const int kt = 32 * (warp & 3) + lane;        // TMEM lane owned by this thread
@@ -507,6 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (!final_out && p.fused_combine)
+            merge_tile<HD, NP>(p, b, ht, sb, rows_valid, sidx, warp & 3, lane, smem + C::kOffK, smem + C::kOffP, red,
+                               bar_merge, merge_flag, wc);
         tc_fence_before();
     }
 

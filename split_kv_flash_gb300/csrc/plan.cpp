@@ -125,6 +125,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     if (opts.max_splits < 0 || opts.force_num_splits < 0 || opts.num_sms < 0 ||
         opts.wait_timeout_us < 0)
         return fail(SK_ERR_INVALID_ARG, "negative option");
+    if (opts.combine_mode < SK_COMBINE_AUTO || opts.combine_mode > SK_COMBINE_IN_KERNEL)
+        return fail(SK_ERR_INVALID_ARG, "unknown combine mode");
 
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.sq = q_len; p.d = d;
     p.causal = causal ? 1 : 0;
@@ -214,6 +216,12 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     p.num_splits = 1;
     for (int c : p.splits_b) p.num_splits = std::max(p.num_splits, c);
     p.needs_combine = p.num_splits > 1;
+    // In-kernel merge (decode path): the last split CTA of a tile stages every
+    // split's partial rows of the tile in its K/V rings, so they must fit there.
+    if (p.needs_combine && p.path == SK_PATH_DECODE && opts.combine_mode != SK_COMBINE_KERNEL) {
+        const long long staged = (long long)p.num_splits * p.rows * d * 4;
+        p.fused_combine = staged <= decode_ring_bytes(d, p.kBlockM);
+    }
 
     p.grid_x = p.num_m_blocks;
     p.grid_y = p.head_tiles * p.num_splits;
@@ -225,6 +233,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     size_t off = 256;
     p.echo_off = off;
     off = align_up(off + size_t(p.num_ctas) * 16, 256);
+    p.cnt_off = off;
+    if (p.fused_combine) off = align_up(off + size_t(B) * p.head_tiles * p.num_m_blocks * 4, 256);
     p.lse_off = off;
     if (p.needs_combine) {
         const size_t rows_all = size_t(p.num_splits) * B * Hq * size_t(q_len);
@@ -280,6 +290,8 @@ void plan_to_info(const Plan& p, sk_attn_plan_info* info) {
     info->echo_offset = p.echo_off;
     info->lse_part_offset = p.lse_off;
     info->o_part_offset = p.o_off;
+    info->combine_in_kernel = p.fused_combine ? 1 : 0;
+    info->counter_offset = p.cnt_off;
 }
 
 }  // namespace sk

@@ -16,6 +16,14 @@ constexpr int kDecodeMaxRows = 64;      // decode path: <= 64 packed rows per ti
 constexpr int kDefaultMaxSplits = 128;
 constexpr int kMaxSplits = 128;         // the combine kernel merges at most 128 partials
 
+// Shared-memory rings of the decode kernel (K and V slots of 128 rows), also
+// needed by the scheduler: the in-kernel merge stages a tile's partials there.
+constexpr int decode_stages_k(int hd) { return hd == 128 ? 3 : 4; }
+constexpr int decode_stages_v(int hd, int np) { return hd == 128 ? (np <= 32 ? 3 : 2) : (np <= 32 ? 4 : 3); }
+constexpr int decode_ring_bytes(int hd, int np) {
+    return decode_stages_k(hd) * 128 * hd * 2 + decode_stages_v(hd, np) * 128 * 128 * 2;
+}
+
 struct Plan {
     // problem
     int B = 0, Hq = 0, Hkv = 0, G = 1, sq = 0, d = 0;
@@ -34,12 +42,13 @@ struct Plan {
     int num_splits_policy = 1, num_splits = 1;
     std::vector<int> splits_b;  // [B] per-sequence split counts
     bool needs_combine = false;
+    bool fused_combine = false;  // the partial kernel merges the splits (no combine kernel)
     bool reverse_m = false;
     int grid_x = 0, grid_y = 0, grid_z = 0;
     long long num_ctas = 0;
     int num_sms = 0;
     // workspace
-    size_t ws_bytes = 0, echo_off = 0, lse_off = 0, o_off = 0;
+    size_t ws_bytes = 0, echo_off = 0, cnt_off = 0, lse_off = 0, o_off = 0;
 };
 
 // Builds the plan; on error returns the status and sets *why.

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(sk):
 
 
 def test_version_and_status_strings(sk):
-    assert sk.sk_attn_version() == 100
+    assert sk.sk_attn_version() == 101
     assert sk.sk_attn_status_string(0) == "SK_OK"
     assert sk.sk_attn_status_string(6) == "SK_ERR_DEVICE_TIMEOUT"
     assert sk.sk_attn_status_string(99) == "SK_ERR_UNKNOWN"
@@ -122,3 +122,25 @@ def test_binding_checks_kv_len_length(sk):
     with pytest.raises(ValueError):
         sk.sk_attn_fwd_noalloc(0, 0, 0, 0, 0, 2, 4, 4, 1, [100, 1, 2], 128, 0.1, 0, -1)
     assert sk.sk_attn_plan(2, 4, 4, 1, [100, 200], 128, opts=o).num_ctas >= 2
+
+
+def test_combine_mode_in_plan(sk):
+    """In-kernel merge: chosen on the decode path when the tile's staged partials
+    fit the decode kernel's K/V rings; never on the prefill path; mode 1 keeps
+    the separate kernel; an unknown mode is rejected."""
+    o = _opts(sk, num_sms=152)
+    info = sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=o)
+    assert info.needs_combine == 1 and info.combine_in_kernel == 1
+    assert info.counter_offset % 256 == 0 and info.lse_part_offset >= info.counter_offset + 4 * 4
+    o1 = _opts(sk, num_sms=152, combine_mode=1)
+    assert sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=o1).combine_in_kernel == 0
+    op = _opts(sk, num_sms=152, force_num_splits=4, force_path=2)
+    assert sk.sk_attn_plan(1, 4, 2, 300, [4000], 128, True, opts=op).combine_in_kernel == 0
+    # 64 rows x 128 splits x 512 B = 4 MB of partials cannot be staged
+    big = _opts(sk, num_sms=152, force_num_splits=128)
+    info = sk.sk_attn_plan(1, 64, 1, 1, [1 << 17], 128, opts=big)
+    assert info.needs_combine == 1 and info.combine_in_kernel == 0
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_attn_plan(1, 32, 4, 1, [4096], 128, opts=_opts(sk, combine_mode=5))
+    assert ei.value.status == 1
+    assert sk.sk_attn_version() == 101

@@ -185,3 +185,45 @@ def test_rows_past_a_sequence_never_leak(sk, case):
         ref_o, ref_l = oracle.attn_fwd(wl.bits(qb), wl.bits(kb), wl.bits(vb), wb.kv_len, wb.scale,
                                        wb.causal, wb.window_left)
         H.compare_full(out[b:b + 1], lse[b:b + 1], ref_o, ref_l, "%s_seq%d" % (name, b))
+
+
+# ------------------------------------------------------- how splits are merged
+
+MERGE_CASES = [
+    wl.tiny_decode(),
+    wl.gqa_decode(16384),
+    wl.gqa_decode(131072),
+    wl.spec_verify(33, 2048),
+    wl.varlen_decode(8),
+    wl.Workload("decode_d64_gqa_empty", 3, 8, 2, 64, 1, [0, 129, 1000], seed=78),
+]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("w", MERGE_CASES, ids=[w.name for w in MERGE_CASES])
+def test_split_merge_modes(sk, w, mode):
+    """The separate combine kernel (mode 1) and the in-kernel merge by the last
+    split CTA of each tile (mode 2) both match the oracle, on two calls in a
+    row over one workspace (the per-tile arrival counters reset themselves)."""
+    opts = sk.Opts()
+    opts.combine_mode = mode
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left, opts)
+    if mode == 2:
+        assert info.combine_in_kernel == int(info.needs_combine == 1)
+    else:
+        assert info.combine_in_kernel == 0
+    q, k, v = wl.make_inputs(w)
+    qg, kg, vg = H.to_gpu(q, k, v)
+    ref_o, ref_l = H.oracle_full(w, q, k, v)
+    out, lse, ws = sk.attn_fwd(qg, kg, vg, w.kv_len, w.scale, w.causal, w.window_left, opts=opts)
+    for call in range(2):
+        if call:
+            out.zero_()
+            lse.zero_()
+            sk.attn_fwd(qg, kg, vg, w.kv_len, w.scale, w.causal, w.window_left, out=out, lse=lse,
+                        workspace=ws, opts=opts)
+        torch.cuda.synchronize()
+        assert sk.sk_attn_workspace_status(ws)[0] == 0
+        H.compare_full(out.float().cpu().numpy().astype(np.float64),
+                       lse.cpu().numpy().astype(np.float64), ref_o, ref_l,
+                       "%s_mode%d_call%d" % (w.name, mode, call))

@@ -79,12 +79,24 @@ typedef enum {
  * fixup of the llama.cpp PR #21086 review, the combine step of the tiling
  * chapter section 5.1). */
 typedef enum {
-    SK_COMBINE_AUTO = 0,      /* the library chooses (SK_COMBINE_IN_KERNEL where it applies) */
+    SK_COMBINE_AUTO = 0,      /* the library chooses (currently SK_COMBINE_KERNEL, the faster one) */
     SK_COMBINE_KERNEL = 1,    /* a second kernel merges every split row */
     SK_COMBINE_IN_KERNEL = 2  /* one launch: the last split CTA of a tile to finish merges the
                                  tile's partials (decode path, when they fit its shared memory;
                                  otherwise the second kernel is used) */
 } sk_combine_mode;
+
+/* How the prefill kernel's CTAs take tiles (sk_attn_opts.prefill_schedule;
+ * tiling chapter section 4.2 single-tile and section 4.4 dynamic persistent
+ * schedulers). */
+typedef enum {
+    SK_SCHEDULE_AUTO = 0,        /* persistent where it applies */
+    SK_SCHEDULE_ONE_TILE = 1,    /* one CTA per tile */
+    SK_SCHEDULE_PERSISTENT = 2   /* one CTA per SM, tiles from an atomic counter, longest first,
+                                    in L2 sections of heads; needs Q rows that are whole groups of
+                                    the 128-row TMA box (128 % heads per group == 0), else one tile
+                                    per CTA */
+} sk_prefill_schedule;
 
 /* Options; an all-zero struct (or NULL) selects the defaults. */
 typedef struct {
@@ -101,6 +113,7 @@ typedef struct {
     void* event_begin;     /* optional cudaEvent_t recorded just before the partial kernel */
     void* event_end;       /* optional cudaEvent_t recorded just after it */
     int combine_mode;      /* sk_combine_mode */
+    int prefill_schedule;  /* sk_prefill_schedule */
 } sk_attn_opts;
 
 /* The host scheduler's decisions for one problem. */
@@ -123,7 +136,11 @@ typedef struct {
     size_t lse_part_offset;   /* byte offset of LSE partials [S][B][Hq][q_len] fp32 */
     size_t o_part_offset;     /* byte offset of O partials [S][B][Hq][q_len][d] fp32 */
     int combine_in_kernel;    /* 1: the partial kernel merges the splits itself (no second launch) */
-    size_t counter_offset;    /* byte offset of the per-tile arrival counters [tiles] uint32 */
+    size_t counter_offset;    /* byte offset of the counters: per-tile arrivals (in-kernel merge) or
+                                 the persistent scheduler's next-tile and finished-CTA counts */
+    int persistent;           /* 1: the prefill kernel runs persistent CTAs */
+    int persistent_ctas;      /* CTAs of the persistent launch (<= SM count) */
+    int l2_section_heads;     /* head tiles per L2 section of the persistent tile order */
 } sk_attn_plan_info;
 
 /* Plan only (host, no device work).  Fills *info.  Same argument meaning as

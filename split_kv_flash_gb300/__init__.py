@@ -16,7 +16,8 @@ __all__ = [
     "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_status_string",
     "sk_attn_fwd_noalloc", "sk_attn_noalloc_status", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
-    "SK_PATH_PREFILL", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
+    "SK_PATH_PREFILL", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
+    "SK_SCHEDULE_ONE_TILE", "SK_SCHEDULE_PERSISTENT", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
 ]
 
@@ -29,6 +30,7 @@ SK_POLICY_DEFAULT, SK_POLICY_FILL, SK_POLICY_FA_HEURISTIC = 0, 1, 2
 SK_POLICY_FIXED_CHUNK, SK_POLICY_MIN_CHUNK = 3, 4
 SK_PATH_AUTO, SK_PATH_DECODE, SK_PATH_PREFILL = 0, 1, 2
 SK_COMBINE_AUTO, SK_COMBINE_KERNEL, SK_COMBINE_IN_KERNEL = 0, 1, 2
+SK_SCHEDULE_AUTO, SK_SCHEDULE_ONE_TILE, SK_SCHEDULE_PERSISTENT = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 16 << 20  # SK_NOALLOC_SCRATCH_BYTES in include/sk_attn.h
 
 
@@ -40,7 +42,7 @@ class Opts(ctypes.Structure):
         ("debug_echo_plan", ctypes.c_int), ("wait_timeout_us", ctypes.c_int),
         ("debug_inject_stall", ctypes.c_int),
         ("event_begin", ctypes.c_void_p), ("event_end", ctypes.c_void_p),
-        ("combine_mode", ctypes.c_int),
+        ("combine_mode", ctypes.c_int), ("prefill_schedule", ctypes.c_int),
     ]
 
 
@@ -55,7 +57,8 @@ class PlanInfo(ctypes.Structure):
         ("needs_combine", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("echo_offset", ctypes.c_size_t), ("lse_part_offset", ctypes.c_size_t),
         ("o_part_offset", ctypes.c_size_t), ("combine_in_kernel", ctypes.c_int),
-        ("counter_offset", ctypes.c_size_t),
+        ("counter_offset", ctypes.c_size_t), ("persistent", ctypes.c_int),
+        ("persistent_ctas", ctypes.c_int), ("l2_section_heads", ctypes.c_int),
     ]
 
     def as_dict(self):

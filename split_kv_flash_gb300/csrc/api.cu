@@ -127,7 +127,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ---- per-thread cache of plans and tensor maps
 struct CallKey {
     int dev, B, Hq, Hkv, q_len, d, causal, window_left;
-    int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms, combine_mode, unused;
+    int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms, combine_mode, prefill_schedule;
     const void *q, *k, *v, *out;
 };
 
@@ -265,6 +265,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     key.policy = o.policy; key.force_num_splits = o.force_num_splits; key.force_pack_gqa = o.force_pack_gqa;
     key.force_path = o.force_path; key.max_splits = o.max_splits; key.num_sms = o.num_sms;
     key.combine_mode = o.combine_mode;
+    key.prefill_schedule = o.prefill_schedule;
     key.q = q; key.k = k; key.v = v; key.out = out;
     const CallEntry* ce = kv_len_host ? lookup_call(key, kv_len_host) : nullptr;
     if (!ce) {
@@ -298,7 +299,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
         fresh.q_tma = p.path == SK_PATH_PREFILL && 128 % fresh.q_gp == 0 && q_rows < (1LL << 31);
         if (fresh.q_tma && !make_q_map(&fresh.tmQ, q, q_rows, Hq, d, fresh.q_gp))
             return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (Q)");
-        fresh.o_tma = fresh.q_tma && !p.needs_combine;
+        fresh.o_tma = fresh.q_tma && !p.needs_combine && !p.persistent;
         if (fresh.o_tma && !make_o_map(&fresh.tmO, out, B, q_len, Hq, d, fresh.q_gp))
             return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (O)");
         ce = insert_call(key, std::move(fresh));
@@ -349,8 +350,12 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     cudaError_t e;
     if (o.event_begin && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_begin), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
-    e = (p.path == SK_PATH_DECODE) ? launch_decode(p, fp, tmK, tmV, stream)
-                                   : launch_prefill(p, fp, tmK, tmV, tmQ, tmO, stream);
+    if (p.path == SK_PATH_DECODE)
+        e = launch_decode(p, fp, tmK, tmV, stream);
+    else if (p.persistent && q_tma)
+        e = launch_prefill_persistent(p, fp, tmK, tmV, tmQ, stream);
+    else
+        e = launch_prefill(p, fp, tmK, tmV, tmQ, tmO, stream);
     if (e != cudaSuccess) return fail_cuda(e, "partial kernel launch");
     if (o.event_end && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_end), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");

@@ -127,6 +127,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
         return fail(SK_ERR_INVALID_ARG, "negative option");
     if (opts.combine_mode < SK_COMBINE_AUTO || opts.combine_mode > SK_COMBINE_IN_KERNEL)
         return fail(SK_ERR_INVALID_ARG, "unknown combine mode");
+    if (opts.prefill_schedule < SK_SCHEDULE_AUTO || opts.prefill_schedule > SK_SCHEDULE_PERSISTENT)
+        return fail(SK_ERR_INVALID_ARG, "unknown prefill schedule");
 
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.sq = q_len; p.d = d;
     p.causal = causal ? 1 : 0;
@@ -216,11 +218,34 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     p.num_splits = 1;
     for (int c : p.splits_b) p.num_splits = std::max(p.num_splits, c);
     p.needs_combine = p.num_splits > 1;
-    // In-kernel merge (decode path): the last split CTA of a tile stages every
-    // split's partial rows of the tile in its K/V rings, so they must fit there.
-    if (p.needs_combine && p.path == SK_PATH_DECODE && opts.combine_mode != SK_COMBINE_KERNEL) {
+    // In-kernel merge (decode path, on request): the last split CTA of a tile
+    // stages every split's partial rows of the tile in its K/V rings, so they
+    // must fit there.  The default keeps the separate combine kernel, which
+    // measured faster (it merges a tile's rows on many SMs at once).
+    if (p.needs_combine && p.path == SK_PATH_DECODE && opts.combine_mode == SK_COMBINE_IN_KERNEL) {
         const long long staged = (long long)p.num_splits * p.rows * d * 4;
         p.fused_combine = staged <= decode_ring_bytes(d, p.kBlockM);
+    }
+
+    // Persistent prefill (tiling chapter sections 4.3-4.4): one CTA per SM over
+    // the tile list, when Q halves can come by TMA (whole 128-row boxes).
+    {
+        const int gp = p.pack_gqa ? p.G : 1;
+        const long long tiles = (long long)p.num_m_blocks * p.head_tiles * p.num_splits * B;
+        p.persistent = p.path == SK_PATH_PREFILL && opts.prefill_schedule != SK_SCHEDULE_ONE_TILE &&
+                       128 % gp == 0 && (long long)B * q_len < (1LL << 31) && tiles > 0 && tiles < (1LL << 30);
+        if (p.persistent) {
+            p.persistent_ctas = int(std::min<long long>(tiles, p.num_sms));
+            // Section 4.4: nearest_power_of_2(32 MB / size of one KV head) heads,
+            // times the query heads per KV head when those are separate tiles
+            // (power of two taken downwards, so that a section fits the budget).
+            const long long kv_head_bytes = std::max<long long>(1, (long long)p.max_kv * (2LL * d) * 2);
+            long long per = (32LL << 20) / kv_head_bytes;
+            long long pow2 = 1;
+            while (pow2 * 2 <= per) pow2 *= 2;
+            const long long sec = pow2 * (p.pack_gqa ? 1 : p.G);
+            p.l2_section = int(std::max<long long>(1, std::min<long long>(sec, (long long)B * p.head_tiles)));
+        }
     }
 
     p.grid_x = p.num_m_blocks;
@@ -235,6 +260,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     off = align_up(off + size_t(p.num_ctas) * 16, 256);
     p.cnt_off = off;
     if (p.fused_combine) off = align_up(off + size_t(B) * p.head_tiles * p.num_m_blocks * 4, 256);
+    if (p.persistent) off = align_up(off + 2 * 4, 256);
     p.lse_off = off;
     if (p.needs_combine) {
         const size_t rows_all = size_t(p.num_splits) * B * Hq * size_t(q_len);
@@ -292,6 +318,9 @@ void plan_to_info(const Plan& p, sk_attn_plan_info* info) {
     info->o_part_offset = p.o_off;
     info->combine_in_kernel = p.fused_combine ? 1 : 0;
     info->counter_offset = p.cnt_off;
+    info->persistent = p.persistent ? 1 : 0;
+    info->persistent_ctas = p.persistent_ctas;
+    info->l2_section_heads = p.l2_section;
 }
 
 }  // namespace sk

@@ -43,6 +43,9 @@ struct Plan {
     std::vector<int> splits_b;  // [B] per-sequence split counts
     bool needs_combine = false;
     bool fused_combine = false;  // the partial kernel merges the splits (no combine kernel)
+    bool persistent = false;     // prefill: one CTA per SM walking the tile list
+    int persistent_ctas = 0;
+    int l2_section = 1;          // head tiles per L2 section of the persistent tile order
     bool reverse_m = false;
     int grid_x = 0, grid_y = 0, grid_z = 0;
     long long num_ctas = 0;

@@ -125,22 +125,45 @@ def test_binding_checks_kv_len_length(sk):
 
 
 def test_combine_mode_in_plan(sk):
-    """In-kernel merge: chosen on the decode path when the tile's staged partials
-    fit the decode kernel's K/V rings; never on the prefill path; mode 1 keeps
-    the separate kernel; an unknown mode is rejected."""
+    """In-kernel merge: on request (mode 2), on the decode path when the tile's
+    staged partials fit the decode kernel's K/V rings; never on the prefill
+    path; the default and mode 1 keep the separate kernel; an unknown mode is
+    rejected."""
     o = _opts(sk, num_sms=152)
+    assert sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=o).combine_in_kernel == 0  # default
+    o = _opts(sk, num_sms=152, combine_mode=2)
     info = sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=o)
     assert info.needs_combine == 1 and info.combine_in_kernel == 1
     assert info.counter_offset % 256 == 0 and info.lse_part_offset >= info.counter_offset + 4 * 4
     o1 = _opts(sk, num_sms=152, combine_mode=1)
     assert sk.sk_attn_plan(1, 32, 4, 1, [131072], 128, opts=o1).combine_in_kernel == 0
-    op = _opts(sk, num_sms=152, force_num_splits=4, force_path=2)
+    op = _opts(sk, num_sms=152, force_num_splits=4, force_path=2, combine_mode=2)
     assert sk.sk_attn_plan(1, 4, 2, 300, [4000], 128, True, opts=op).combine_in_kernel == 0
     # 64 rows x 128 splits x 512 B = 4 MB of partials cannot be staged
-    big = _opts(sk, num_sms=152, force_num_splits=128)
+    big = _opts(sk, num_sms=152, force_num_splits=128, combine_mode=2)
     info = sk.sk_attn_plan(1, 64, 1, 1, [1 << 17], 128, opts=big)
     assert info.needs_combine == 1 and info.combine_in_kernel == 0
     with pytest.raises(sk.SKError) as ei:
         sk.sk_attn_plan(1, 32, 4, 1, [4096], 128, opts=_opts(sk, combine_mode=5))
     assert ei.value.status == 1
     assert sk.sk_attn_version() == 101
+
+
+def test_persistent_prefill_plan(sk):
+    """Prefill plans run persistent CTAs (at most one per SM) unless told not
+    to; the L2 section follows the 32 MB rule; G = 3 (a 128-row box is not whole
+    head groups) keeps one CTA per tile."""
+    o = _opts(sk, num_sms=152)
+    info = sk.sk_attn_plan(4, 32, 8, 8192, [8192] * 4, 128, True, opts=o)
+    assert info.persistent == 1 and info.persistent_ctas == 152
+    # one KV head of 8192 keys = 8192 * 256 * 2 B = 4 MB -> 8 KV heads, x G = 4 query heads
+    assert info.l2_section_heads == 32
+    assert info.counter_offset % 256 == 0 and info.lse_part_offset >= info.counter_offset + 8
+    assert sk.sk_attn_plan(4, 32, 8, 8192, [8192] * 4, 128, True,
+                           opts=_opts(sk, num_sms=152, prefill_schedule=1)).persistent == 0
+    assert sk.sk_attn_plan(1, 6, 2, 300, [500], 128, True, opts=o).persistent == 0  # G = 3
+    small = sk.sk_attn_plan(1, 2, 2, 300, [300], 128, True, opts=o)
+    assert small.persistent == 1 and small.persistent_ctas == small.num_ctas  # fewer tiles than SMs
+    assert sk.sk_attn_plan(1, 32, 4, 1, [4096], 128, opts=o).persistent == 0  # decode path
+    with pytest.raises(sk.SKError):
+        sk.sk_attn_plan(1, 2, 2, 300, [300], 128, True, opts=_opts(sk, prefill_schedule=7))

@@ -227,3 +227,49 @@ def test_split_merge_modes(sk, w, mode):
         H.compare_full(out.float().cpu().numpy().astype(np.float64),
                        lse.cpu().numpy().astype(np.float64), ref_o, ref_l,
                        "%s_mode%d_call%d" % (w.name, mode, call))
+
+
+# --------------------------------------------------- prefill tile schedules
+
+SCHED_CASES = [
+    # name, B, Hq, Hkv, d, q_len, kv_len, causal, window, forced splits
+    ("causal_multi_tile", 2, 4, 2, 128, 700, [700, 700], True, -1, 0),
+    ("local_window", 1, 8, 2, 128, 1100, [1100], True, 130, 0),
+    ("varlen_splits", 3, 4, 2, 128, 300, [2000, 300, 900], True, -1, 3),
+    ("packed_gqa_d64", 1, 16, 2, 64, 40, [3000], False, -1, 0),
+    ("sk_lt_sq", 1, 2, 2, 128, 600, [150], True, -1, 0),
+    ("window_no_causal", 1, 2, 2, 128, 400, [900], False, 60, 2),
+]
+
+
+@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("case", SCHED_CASES, ids=[c[0] for c in SCHED_CASES])
+def test_prefill_schedules(sk, case, schedule):
+    """One CTA per tile (1) and persistent CTAs taking tiles from the atomic
+    counter (2) give the oracle's result, twice in a row on one workspace (the
+    persistent counters re-arm themselves), and echo the host plan's ranges."""
+    name, B, Hq, Hkv, d, sq, kv, causal, window, S = case
+    w = wl.Workload(name, B, Hq, Hkv, d, sq, kv, causal=causal, window_left=window, seed=41)
+    opts = sk.Opts()
+    opts.prefill_schedule = schedule
+    opts.force_path = sk.SK_PATH_PREFILL
+    opts.debug_echo_plan = 1
+    if S:
+        opts.force_num_splits = S
+    info = sk.sk_attn_plan(B, Hq, Hkv, sq, kv, d, causal, window, opts)
+    assert info.persistent == (1 if schedule == 2 else 0)
+    q, k, v = wl.make_inputs(w)
+    qg, kg, vg = H.to_gpu(q, k, v)
+    ref_o, ref_l = H.oracle_full(w, q, k, v)
+    out, lse, ws = sk.attn_fwd(qg, kg, vg, kv, w.scale, causal, window, opts=opts)
+    for call in range(2):
+        if call:
+            out.zero_()
+            sk.attn_fwd(qg, kg, vg, kv, w.scale, causal, window, out=out, lse=lse, workspace=ws, opts=opts)
+        torch.cuda.synchronize()
+        assert sk.sk_attn_workspace_status(ws)[0] == 0
+        H.compare_full(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                       ref_o, ref_l, "%s_sched%d_call%d" % (name, schedule, call))
+    echo = sk.sk_attn_read_plan_echo(ws, info.num_ctas)
+    host = sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, opts)
+    assert np.array_equal(np.array(echo, dtype=np.int32), np.array(host, dtype=np.int32))

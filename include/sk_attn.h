@@ -90,7 +90,7 @@ typedef enum {
  * tiling chapter section 4.2 single-tile and section 4.4 dynamic persistent
  * schedulers). */
 typedef enum {
-    SK_SCHEDULE_AUTO = 0,        /* persistent where it applies */
+    SK_SCHEDULE_AUTO = 0,        /* the library chooses (currently one CTA per tile, measured faster) */
     SK_SCHEDULE_ONE_TILE = 1,    /* one CTA per tile */
     SK_SCHEDULE_PERSISTENT = 2   /* one CTA per SM, tiles from an atomic counter, longest first,
                                     in L2 sections of heads; needs Q rows that are whole groups of

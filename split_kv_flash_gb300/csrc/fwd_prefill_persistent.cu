@@ -452,29 +452,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             float l_run = 0.f;
             for (int i = 0; i < cnt; ++i) {
                 const int n = hi_t - 1 - i;
-                float x[128];
                 mbar_wait(bar_sfull(t), s_cnt & 1, wc, (kKernPrefill << 8) | kSiteSoftmaxSFull);
                 ++s_cnt;
                 tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < 8; ++c) tmem_ld16(tS(t) + lane_off + c * 16, x + c * 16);
-                tmem_wait_ld();
                 const int blk_first = n * 128, blk_last = n * 128 + 127;
                 const bool need_mask = (blk_last >= sk) || (has_causal && blk_last > diag_lo) ||
                                        (has_window && blk_first < diag_hi - p.window_left) || rows_valid < 128;
-                if (need_mask) {
-                    const int c_lo = key_lo - blk_first, c_hi = key_hi - blk_first;
+                const int c_lo = key_lo - blk_first, c_hi = key_hi - blk_first;
+                // Two passes over the scores in TMEM, 32 columns at a time, so that
+                // a row's 128 scores never sit in registers at once (this warp's
+                // state lives across tiles).  Pass 1: the row max.
+                float mx = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+                for (int c = 0; c < 4; ++c) {
+                    float x[32];
+                    tmem_ld16(tS(t) + lane_off + c * 32, x);
+                    tmem_ld16(tS(t) + lane_off + c * 32 + 16, x + 16);
+                    tmem_wait_ld();
+                    if (need_mask) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c * 32 + e < c_lo || c * 32 + e > c_hi) x[e] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, x[e]);
                 }
-                float mx8[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) mx8[c] = x[c];
-#pragma unroll
-                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float cand = mx * sl2;
                 bool rescale = false;
                 float alpha = 1.f;
@@ -499,13 +501,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // Pass 2: P = 2^(s * x - m) as packed bf16 pairs over the upper half
+                // of S_t.  Chunks run from the last one down: chunk c's P lands on
+                // the scores of chunks c + 1 .. 3 (already consumed), never on
+                // scores still to be read.
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int c4 = 3; c4 >= 0; --c4) {
+                    float x[32];
+                    tmem_ld16(tS(t) + lane_off + c4 * 32, x);
+                    tmem_ld16(tS(t) + lane_off + c4 * 32 + 16, x + 16);
+                    tmem_wait_ld();
+                    if (need_mask) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c4 * 32 + e < c_lo || c4 * 32 + e > c_hi) x[e] = -INFINITY;
+                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = fast_exp2(fmaf(x[c4 * 32 + 2 * e], sl2, neg_m));
-                        const float p1 = fast_exp2(fmaf(x[c4 * 32 + 2 * e + 1], sl2, neg_m));
+                        const float p0 = fast_exp2(fmaf(x[2 * e], sl2, neg_m));
+                        const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl2, neg_m));
                         ls[(2 * e) & 3] += p0;
                         ls[(2 * e + 1) & 3] += p1;
                         pk[e] = pack_bf16x2(p0, p1);

@@ -232,7 +232,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     {
         const int gp = p.pack_gqa ? p.G : 1;
         const long long tiles = (long long)p.num_m_blocks * p.head_tiles * p.num_splits * B;
-        p.persistent = p.path == SK_PATH_PREFILL && opts.prefill_schedule != SK_SCHEDULE_ONE_TILE &&
+        p.persistent = p.path == SK_PATH_PREFILL && opts.prefill_schedule == SK_SCHEDULE_PERSISTENT &&
                        128 % gp == 0 && (long long)B * q_len < (1LL << 31) && tiles > 0 && tiles < (1LL << 30);
         if (p.persistent) {
             p.persistent_ctas = int(std::min<long long>(tiles, p.num_sms));

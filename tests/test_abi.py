@@ -150,10 +150,11 @@ def test_combine_mode_in_plan(sk):
 
 
 def test_persistent_prefill_plan(sk):
-    """Prefill plans run persistent CTAs (at most one per SM) unless told not
-    to; the L2 section follows the 32 MB rule; G = 3 (a 128-row box is not whole
-    head groups) keeps one CTA per tile."""
-    o = _opts(sk, num_sms=152)
+    """Prefill plans run persistent CTAs (at most one per SM) on request; the L2
+    section follows the 32 MB rule; G = 3 (a 128-row box is not whole head
+    groups) keeps one CTA per tile."""
+    assert sk.sk_attn_plan(4, 32, 8, 8192, [8192] * 4, 128, True, opts=_opts(sk, num_sms=152)).persistent == 0
+    o = _opts(sk, num_sms=152, prefill_schedule=2)
     info = sk.sk_attn_plan(4, 32, 8, 8192, [8192] * 4, 128, True, opts=o)
     assert info.persistent == 1 and info.persistent_ctas == 152
     # one KV head of 8192 keys = 8192 * 256 * 2 B = 4 MB -> 8 KV heads, x G = 4 query heads

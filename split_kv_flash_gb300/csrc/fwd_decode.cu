@@ -13,10 +13,10 @@
 // normalised partial O and log-sum-exp for the combine kernel, or the final
 // output when the sequence has a single split.
 //
-// Warp roles (224 threads): warps 0 and 6 issue the TMA loads of K and of V
-// blocks into two multi-stage shared-memory rings; warp 1 owns TMEM and issues
-// the MMAs; warps 2-5 (128 threads, thread t <-> TMEM lane t = key t of S^T and
-// d-row t of O^T) do the softmax, the rescaling and the epilogue.
+// Warp roles (192 threads): warp 0 issues the TMA loads of K and V blocks into
+// two multi-stage shared-memory rings; warp 1 owns TMEM and issues the MMAs;
+// warps 2-5 (128 threads, thread t <-> TMEM lane t = key t of S^T and d-row t
+// of O^T) do the softmax, the rescaling and the epilogue.
 #include <math.h>
 
 #include "fwd_common.cuh"
@@ -26,7 +26,7 @@
 namespace sk {
 namespace {
 
-constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
+constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -291,16 +291,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 2 * NP;   // O^T: columns [2NP, 3NP)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
-    if (warp == 0 || warp == 6) {
-        // ===================== TMA producers: warp 0 streams K, warp 6 streams V,
-        // each into its own ring (whole warp runs the loop, one elected lane
-        // issues the copies).
+    if (warp == 0) {
+        // ===================== TMA producer (K and V rings): the whole warp
+        // runs the loop, one elected lane issues the copies.  (One warp per
+        // tensor, with K never queued behind a V slot, measured no faster.)
         const bool leader = elect_one();
+        const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
+        const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
         const int kvh = p.pack_gqa ? ht : ht / p.G;
-        const KvRing ring = warp == 0 ? KvRing{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST}
-                                      : KvRing{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
-        produce_ring<HD>(warp == 0 ? &tmK : &tmV, ring, nblocks, kvh * HD, kv_off + br.lo * 128, false,
-                         l2_policy_evict_first(), wc, (kKernDecode << 8) | kSiteProducerEmpty, leader);
+        produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, false, l2_policy_evict_first(), wc,
+                       (kKernDecode << 8) | kSiteProducerEmpty, leader);
     } else if (warp == 1) {
         // ===================== MMA issuer
         // The whole warp runs the schedule (warp-uniform control flow and
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (leader) umma_commit(bar_drain);
         mbar_drain(bar_drain, 0, p.timeout_ns);
-    } else if (warp >= 2 && warp <= 5) {
+    } else {
         // ===================== softmax / correction / epilogue (128 threads)
         const int sidx = threadIdx.x - 64;            // 0..127 for cooperative loops
         const int kt = 32 * (warp & 3) + lane;        // TMEM lane owned by this thread

@@ -4,13 +4,9 @@
 // soon as its PV MMAs have, so K runs ahead of V and the next QK^T never waits
 // for a whole K+V load.
 //
-// Two forms:
-//  - produce_ring: one warp per tensor (the decode kernel).  Each ring is
-//    refilled the moment a slot frees, so a K load never waits behind a V slot.
-//  - produce_kv: one warp for both (the prefill kernel).  The MMA warp issues
-//    QK^T(j) before the last PV(j-1), so the slots free up in the order K(j),
-//    V(j-1), K(j+1), V(j), ...; the producer waits for them in exactly that
-//    order.
+// One warp streams both: the MMA warp issues QK^T(j) before the last PV(j-1),
+// so the slots free up in the order K(j), V(j-1), K(j+1), V(j), ...; the
+// producer waits for them in exactly that order.
 // All waits are bounded and suspend the thread.  The whole producer warp runs
 // these loops (warp-uniform control flow); one elected lane, `leader`, issues
 // the copies.  A ring position counts the blocks loaded so far: slot
@@ -95,20 +91,6 @@ __device__ __forceinline__ void zero_rows(uint32_t slot, int first, int lane) {
 __device__ __forceinline__ void drain_ring(const KvRing& R, int loaded, uint64_t limit_ns) {
     for (int pos = loaded - 1; pos >= 0 && pos >= loaded - R.slots; --pos)
         mbar_drain(R.full + 8u * (pos % R.slots), (pos / R.slots) & 1, limit_ns);
-}
-
-// One tensor's blocks (rows y0 + 128 * visit_block(j), j in [0, nblocks)) into
-// its own ring, then drain what was issued.  With K and V each streamed by its
-// own warp, a K load never queues behind a V slot that is still being read.
-template <int HD>
-__device__ __forceinline__ void produce_ring(const CUtensorMap* tm, const KvRing& R, int nblocks, int x0, int y0,
-                                             bool desc, uint64_t policy, const WaitCtl& wc, int where, bool leader) {
-    int loaded = 0;
-    for (int j = 0; j < nblocks; ++j) {
-        if (!load_block<HD>(tm, R, j, x0, y0 + visit_block(j, nblocks, desc) * 128, policy, wc, where, leader)) break;
-        loaded = j + 1;
-    }
-    drain_ring(R, loaded, wc.limit_ns);
 }
 
 // Single-tile form: stream one range, then drain what was issued.

@@ -42,6 +42,15 @@ def lib():
                                             ctypes.c_double, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int, i32p, f64p, f64p, ctypes.c_int]
         L.oracle_attn_fwd_split.restype = ctypes.c_int
+        L.oracle_attn_rows_v.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                         ctypes.c_int, ctypes.c_int, i32p, ctypes.c_long, f64p,
+                                         f64p, ctypes.c_int]
+        L.oracle_attn_rows_v.restype = ctypes.c_int
+        L.oracle_attn_fwd_v.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                        ctypes.c_int, ctypes.c_int, f64p, f64p, ctypes.c_int]
+        L.oracle_attn_fwd_v.restype = ctypes.c_int
         L.oracle_count_visible.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.oracle_count_visible.restype = ctypes.c_longlong
         _lib = L
@@ -123,6 +132,50 @@ def attn_fwd_split(q, k, v, kv_len, scale, bounds, causal=False, window_left=-1,
                                      _f64p(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd_split rejected its arguments")
+    return out, lse
+
+
+def attn_fwd_v(q, k, v, kv_len, scale, causal=False, window_left=-1, nthreads=0):
+    """Full fp64 attention with value width dv (the last dimension of v) that may
+    differ from the query/key width d.  q [B, sq, Hq, d]; k [sum(kv_len), Hkv, d];
+    v [sum(kv_len), Hkv, dv], all uint16 bf16 bits.  Returns (out [B, sq, Hq, dv],
+    lse [B, Hq, sq]) as float64."""
+    B, sq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    dv = v.shape[2]
+    if k.shape[2] != d or v.shape[:2] != k.shape[:2]:
+        raise ValueError("shape mismatch")
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    kl, klp = _i32(kv_len)
+    out = np.zeros((B, sq, Hq, dv), dtype=np.float64)
+    lse = np.zeros((B, Hq, sq), dtype=np.float64)
+    rc = lib().oracle_attn_fwd_v(qp, kp, vp, B, Hq, Hkv, sq, klp, d, dv, float(scale), int(causal),
+                                 int(window_left), _f64p(out), _f64p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_v rejected its arguments")
+    return out, lse
+
+
+def attn_rows_v(q, k, v, kv_len, scale, rows, causal=False, window_left=-1, nthreads=0):
+    """Selected rows (int array [n, 3] of (b, h, i)) with value width dv = v.shape[2].
+    Returns (out [n, dv] float64, lse [n] float64)."""
+    B, sq, Hq, d = q.shape
+    Hkv = k.shape[1]
+    dv = v.shape[2]
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    kl, klp = _i32(kv_len)
+    rows, rp = _i32(np.asarray(rows).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.zeros((n, dv), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = lib().oracle_attn_rows_v(qp, kp, vp, B, Hq, Hkv, sq, klp, d, dv, float(scale), int(causal),
+                                  int(window_left), rp, n, _f64p(out), _f64p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_v rejected its arguments")
     return out, lse
 
 

@@ -27,6 +27,9 @@
  *   LSE   = ln sum_j exp(x_j)     (evaluated as M + ln sum exp(x_j - M), M = max x_j)
  *   O     = sum_j exp(x_j - LSE) * V[off_b + j, hk, :]
  *   no visible key -> O = 0, LSE = -inf.
+ * Keys and queries have d columns, values and outputs dv (dv = d except for the
+ * latent-attention entry points: "The Occupancy Awakening", the absorbed-MLA
+ * verify of Kimi K2.6 with 512 + 64 query/key columns and 512 value columns).
  *
  * Everything is double precision.  Inputs arrive as raw bf16 bit patterns
  * (uint16), widened exactly to double.  No tiling, no online rescaling: the
@@ -60,9 +63,9 @@ static int key_visible(long i, long j, long sq, long sk, int causal, long wl) {
 }
 
 /* One output row restricted to keys in [j_lo, j_hi) (all keys: 0, sk).
- * Writes d doubles to o_row and returns the log-sum-exp. */
+ * Writes dv doubles to o_row and returns the log-sum-exp. */
 static double attn_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                       int Hq, int Hkv, int sq, int d, double scale, int causal,
+                       int Hq, int Hkv, int sq, int d, int dv, double scale, int causal,
                        int wl, long b, long h, long i, long sk, long off,
                        long j_lo, long j_hi, double* logits, double* o_row) {
     const long G = Hq / Hkv;
@@ -86,7 +89,7 @@ static double attn_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         if (x > mx) mx = x;
         ++nvis;
     }
-    for (int c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (int c = 0; c < dv; ++c) o_row[c] = 0.0;
     if (nvis == 0) return -INFINITY;
     /* 2. softmax normaliser */
     double sum = 0.0;
@@ -101,8 +104,8 @@ static double attn_row(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         double x = logits[j - j_lo];
         if (x == -INFINITY) continue;
         double w = exp(x - lse);
-        const uint16_t* vrow = v + (((size_t)(off + j)) * Hkv + hk) * (size_t)d;
-        for (int c = 0; c < d; ++c) o_row[c] += w * bf16_bits_to_double(vrow[c]);
+        const uint16_t* vrow = v + (((size_t)(off + j)) * Hkv + hk) * (size_t)dv;
+        for (int c = 0; c < dv; ++c) o_row[c] += w * bf16_bits_to_double(vrow[c]);
     }
     return lse;
 }
@@ -117,17 +120,17 @@ static int check_args(int B, int Hq, int Hkv, int sq, const int* kv_len, int d) 
 
 /*
  * Selected rows of the attention output.  rows holds n_rows triples
- * (b, h, i); out_rows receives n_rows x d doubles, lse_rows n_rows doubles.
- * Layouts: q [B, sq, Hq, d]; k, v [sum_b kv_len[b], Hkv, d] packed by
- * sequence (offset of sequence b = sum of the lengths before it).
- * Returns 0, or -1 on bad arguments.
+ * (b, h, i); out_rows receives n_rows x dv doubles, lse_rows n_rows doubles.
+ * Layouts: q [B, sq, Hq, d]; k [sum_b kv_len[b], Hkv, d] and v
+ * [sum_b kv_len[b], Hkv, dv] packed by sequence (offset of sequence b = sum of
+ * the lengths before it).  Returns 0, or -1 on bad arguments.
  */
-int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                     int B, int Hq, int Hkv, int sq, const int* kv_len, int d,
-                     double scale, int causal, int window_left,
-                     const int* rows, long n_rows, double* out_rows, double* lse_rows,
-                     int nthreads) {
-    if (check_args(B, Hq, Hkv, sq, kv_len, d)) return -1;
+int oracle_attn_rows_v(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       int B, int Hq, int Hkv, int sq, const int* kv_len, int d, int dv,
+                       double scale, int causal, int window_left,
+                       const int* rows, long n_rows, double* out_rows, double* lse_rows,
+                       int nthreads) {
+    if (check_args(B, Hq, Hkv, sq, kv_len, d) || dv <= 0) return -1;
     long* off = (long*)malloc(sizeof(long) * (size_t)(B + 1));
     long max_sk = 0;
     off[0] = 0;
@@ -150,9 +153,9 @@ int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 #pragma omp for schedule(dynamic, 4)
         for (long r = 0; r < n_rows; ++r) {
             long b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
-            lse_rows[r] = attn_row(q, k, v, Hq, Hkv, sq, d, scale, causal, window_left, b, h, i,
+            lse_rows[r] = attn_row(q, k, v, Hq, Hkv, sq, d, dv, scale, causal, window_left, b, h, i,
                                    kv_len[b], off[b], 0, kv_len[b], logits,
-                                   out_rows + (size_t)r * d);
+                                   out_rows + (size_t)r * dv);
         }
         free(logits);
     }
@@ -160,17 +163,27 @@ int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     return 0;
 }
 
+/* Keys and values of one width (the common case). */
+int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     int B, int Hq, int Hkv, int sq, const int* kv_len, int d,
+                     double scale, int causal, int window_left,
+                     const int* rows, long n_rows, double* out_rows, double* lse_rows,
+                     int nthreads) {
+    return oracle_attn_rows_v(q, k, v, B, Hq, Hkv, sq, kv_len, d, d, scale, causal, window_left,
+                              rows, n_rows, out_rows, lse_rows, nthreads);
+}
+
 /*
- * Full attention forward: out [B, sq, Hq, d] (double), lse [B, Hq, sq] (double).
+ * Full attention forward: out [B, sq, Hq, dv] (double), lse [B, Hq, sq] (double).
  */
-int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                    int B, int Hq, int Hkv, int sq, const int* kv_len, int d,
-                    double scale, int causal, int window_left,
-                    double* out, double* lse, int nthreads) {
-    if (check_args(B, Hq, Hkv, sq, kv_len, d)) return -1;
+int oracle_attn_fwd_v(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      int B, int Hq, int Hkv, int sq, const int* kv_len, int d, int dv,
+                      double scale, int causal, int window_left,
+                      double* out, double* lse, int nthreads) {
+    if (check_args(B, Hq, Hkv, sq, kv_len, d) || dv <= 0) return -1;
     long n = (long)B * Hq * sq;
     int* rows = (int*)malloc(sizeof(int) * 3 * (size_t)(n > 0 ? n : 1));
-    double* o_rows = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    double* o_rows = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * dv);
     double* l_rows = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     long r = 0;
     for (int b = 0; b < B; ++b)
@@ -178,21 +191,30 @@ int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
             for (int i = 0; i < sq; ++i) {
                 rows[3 * r] = b; rows[3 * r + 1] = h; rows[3 * r + 2] = i; ++r;
             }
-    int rc = oracle_attn_rows(q, k, v, B, Hq, Hkv, sq, kv_len, d, scale, causal, window_left,
-                              rows, n, o_rows, l_rows, nthreads);
+    int rc = oracle_attn_rows_v(q, k, v, B, Hq, Hkv, sq, kv_len, d, dv, scale, causal, window_left,
+                                rows, n, o_rows, l_rows, nthreads);
     if (rc == 0) {
         r = 0;
         for (int b = 0; b < B; ++b)
             for (int h = 0; h < Hq; ++h)
                 for (int i = 0; i < sq; ++i) {
-                    memcpy(out + (((size_t)b * sq + i) * Hq + h) * d, o_rows + (size_t)r * d,
-                           sizeof(double) * d);
+                    memcpy(out + (((size_t)b * sq + i) * Hq + h) * dv, o_rows + (size_t)r * dv,
+                           sizeof(double) * dv);
                     lse[((size_t)b * Hq + h) * sq + i] = l_rows[r];
                     ++r;
                 }
     }
     free(rows); free(o_rows); free(l_rows);
     return rc;
+}
+
+/* Keys and values of one width (the common case). */
+int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    int B, int Hq, int Hkv, int sq, const int* kv_len, int d,
+                    double scale, int causal, int window_left,
+                    double* out, double* lse, int nthreads) {
+    return oracle_attn_fwd_v(q, k, v, B, Hq, Hkv, sq, kv_len, d, d, scale, causal, window_left,
+                             out, lse, nthreads);
 }
 
 /*
@@ -243,7 +265,7 @@ int oracle_attn_fwd_split(const uint16_t* q, const uint16_t* k, const uint16_t* 
             const int* bd = bounds + (size_t)b * (S + 1);
             double mx = -INFINITY;
             for (int t = 0; t < S; ++t) {
-                l_part[t] = attn_row(q, k, v, Hq, Hkv, sq, d, scale, causal, window_left, b, h, i,
+                l_part[t] = attn_row(q, k, v, Hq, Hkv, sq, d, d, scale, causal, window_left, b, h, i,
                                      kv_len[b], off[b], bd[t], bd[t + 1], logits,
                                      o_part + (size_t)t * d);
                 if (l_part[t] > mx) mx = l_part[t];

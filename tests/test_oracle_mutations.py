@@ -32,6 +32,10 @@ MUTATIONS = {
     "bf16_widening_shift": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
     "merge_weight_wrong": ("double w = exp(l_part[t] - total);", "double w = exp(l_part[t] - mx);"),
     "merge_lse_drops_max": ("total = mx + log(acc);", "total = log(acc);"),
+    "value_rows_at_key_stride": ("const uint16_t* vrow = v + (((size_t)(off + j)) * Hkv + hk) * (size_t)dv;",
+                                 "const uint16_t* vrow = v + (((size_t)(off + j)) * Hkv + hk) * (size_t)d;"),
+    "value_width_truncated": ("for (int c = 0; c < dv; ++c) o_row[c] += w * bf16_bits_to_double(vrow[c]);",
+                              "for (int c = 0; c < d && c < dv; ++c) o_row[c] += w * bf16_bits_to_double(vrow[c]);"),
 }
 
 PIN_TESTS = [(n, f) for n, f in inspect.getmembers(pins, inspect.isfunction) if n.startswith("test_")]
@@ -77,7 +81,7 @@ def test_planted_mistake_is_caught(tmp_path, mutation):
     real = oracle.lib()
     mutant = ctypes.CDLL(lib_path)
     for fname in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_attn_fwd_split",
-                  "oracle_count_visible"):
+                  "oracle_count_visible", "oracle_attn_rows_v", "oracle_attn_fwd_v"):
         getattr(mutant, fname).argtypes = getattr(real, fname).argtypes
         getattr(mutant, fname).restype = getattr(real, fname).restype
     oracle._lib = mutant

@@ -306,3 +306,60 @@ def test_local_pair_count_closed_form(oracle_mod):
 
 def test_unmasked_pair_count(oracle_mod):
     assert oracle_mod.count_visible(9, 2065, 0, -1) == 9 * 2065
+
+
+# ------------------------------------------ value width different from key width
+
+def test_value_width_single_key_and_mean(oracle_mod):
+    """dv != d: one visible key returns its dv-wide value row and LSE = s q.k;
+    identical keys return the mean of the dv-wide value rows, LSE + ln n."""
+    rng = np.random.default_rng(21)
+    d, dv = 24, 40
+    q = rand_bits((1, 1, 3, d), rng)
+    k1 = rand_bits((1, 1, d), rng)
+    v1 = rand_bits((1, 1, dv), rng)
+    out, lse = oracle_mod.attn_fwd_v(q, k1, v1, [1], 0.3)
+    qf, kf, vf = as_f64(q), as_f64(k1), as_f64(v1)
+    for h in range(3):
+        np.testing.assert_array_equal(out[0, 0, h], vf[0, 0])
+        assert lse[0, h, 0] == pytest.approx(0.3 * float(qf[0, 0, h] @ kf[0, 0]), rel=1e-12, abs=1e-12)
+    n = 5
+    k = np.repeat(k1, n, axis=0)
+    v = rand_bits((n, 1, dv), rng)
+    out, lse = oracle_mod.attn_fwd_v(q, k, v, [n], 0.3)
+    vf = as_f64(v)
+    np.testing.assert_allclose(out[0, 0, 1], vf[:, 0].mean(axis=0), rtol=0, atol=1e-12)
+    assert lse[0, 1, 0] == pytest.approx(0.3 * float(qf[0, 0, 1] @ kf[0, 0]) + math.log(n), abs=1e-12)
+
+
+def test_latent_values_match_torch_float64(oracle_mod):
+    """Absorbed-MLA form (one latent KV head shared by every query head; the
+    value is the first dv columns of each latent row), causal, against torch
+    float64 softmax on a small case."""
+    rng = np.random.default_rng(22)
+    B, sq, Hq, d, dv, sk = 1, 3, 4, 36, 32, 11
+    q = rand_bits((B, sq, Hq, d), rng)
+    kv = rand_bits((sk, 1, d), rng)
+    v = np.ascontiguousarray(kv[:, :, :dv])
+    out, lse = oracle_mod.attn_fwd_v(q, kv, v, [sk], 0.2, causal=True)
+    qt, kt = torch.from_numpy(as_f64(q)), torch.from_numpy(as_f64(kv))
+    for i in range(sq):
+        n = i + sk - sq + 1
+        for h in range(Hq):
+            x = 0.2 * (kt[:n, 0] @ qt[0, i, h])
+            wts = torch.softmax(x, dim=0)
+            ref = (wts[:, None] * kt[:n, 0, :dv]).sum(dim=0)
+            np.testing.assert_allclose(out[0, i, h], ref.numpy(), rtol=0, atol=1e-12)
+            assert lse[0, h, i] == pytest.approx(float(torch.logsumexp(x, dim=0)), abs=1e-12)
+
+
+def test_value_width_equal_matches_common_entry_point(oracle_mod):
+    """With dv = d the value-width entry point and the common one agree bit for bit."""
+    rng = np.random.default_rng(23)
+    q = rand_bits((2, 4, 4, 16), rng)
+    k = rand_bits((30, 2, 16), rng)
+    v = rand_bits((30, 2, 16), rng)
+    o1, l1 = oracle_mod.attn_fwd(q, k, v, [10, 20], 0.25, True, 5)
+    o2, l2 = oracle_mod.attn_fwd_v(q, k, v, [10, 20], 0.25, True, 5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)

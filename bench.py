@@ -72,6 +72,8 @@ def named_workloads():
     ws["gqa_kv131072"] = wl.gqa_decode(131072)
     ws["prefill_causal"] = wl.prefill(False)
     ws["prefill_local1024"] = wl.prefill(True)
+    for w in latent_workloads():
+        ws[w.name.replace("latent_verify_", "latent_")] = w
     return ws
 
 
@@ -80,6 +82,18 @@ def run_named(sk, name, calls, device):
     drawn on the device; checks the device status word at the end."""
     w = named_workloads()[name]
     g = torch.Generator(device=device).manual_seed(w.seed)
+    if isinstance(w, wl.LatentWorkload):
+        q = torch.randn((w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
+        kv = (torch.randn((w.total_kv, w.d), device=device, generator=g) * w.kv_scale).to(torch.bfloat16)
+        out, lse, ws = sk.attn_fwd_latent(q, kv, w.kv_len, w.scale, w.causal, w.window_left)
+        for _ in range(calls):
+            sk.attn_fwd_latent(q, kv, w.kv_len, w.scale, w.causal, w.window_left, out=out, lse=lse, workspace=ws)
+        torch.cuda.synchronize(device)
+        st, where = sk.sk_attn_workspace_status(ws)
+        if st != 0:
+            raise RuntimeError("device status %d at %d" % (st, where))
+        print(json.dumps({"workload": w.name, "calls": calls + 1, "status": "ok"}), flush=True)
+        return
     q = torch.randn((w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
     k = (torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g) * w.k_scale).to(torch.bfloat16)
     v = torch.randn((w.total_kv, w.Hkv, w.d), device=device, generator=g).to(torch.bfloat16)
@@ -483,6 +497,103 @@ def gpu_sweep(sk, device, hbm_peak, reps=20, warmup=3, loop_reps=10):
     return rows
 
 
+def latent_workloads():
+    """Latent attention (absorbed MLA, one 576-column latent head): the verify
+    shapes of "The Occupancy Awakening" and two longer prefixes at 64 heads."""
+    return [wl.latent_verify(2, 16, 17, 2065), wl.latent_verify(1, 64, 33, 161),
+            wl.latent_verify(2, 64, 9, 521), wl.latent_verify(1, 64, 9, 16384),
+            wl.latent_verify(1, 64, 1, 65536)]
+
+
+def latent_bytes(w):
+    """Latent rows read once (the values are their first 512 columns), Q, O, LSE."""
+    return w.total_kv * w.d * 2 + w.B * w.q_len * w.Hq * (w.d + w.dv) * 2 + w.B * w.Hq * w.q_len * 4
+
+
+def latent_flops(w):
+    """QK^T over 576 columns and PV over 512 per visible (query, key) pair per head."""
+    return 2.0 * (w.d + w.dv) * visible_pairs(w)
+
+
+def gpu_latent_sweep(sk, device, hbm_peak, bf16_peak, reps=20, warmup=3, loop_reps=10):
+    """Lone-call and graph-loop timings of the latent path (same method as the
+    decode sweep), with the tensor and HBM fractions of each."""
+    rows = []
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for w in latent_workloads():
+        nbytes = latent_bytes(w)
+        R = max(1, min(4096, -(-2 * L2_BYTES // max(w.total_kv * w.d * 2, 1))))
+        g = torch.Generator(device=device).manual_seed(w.seed)
+        q = torch.randn((R, w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
+        kv = (torch.randn((R, w.total_kv, w.d), device=device, generator=g) * w.kv_scale).to(torch.bfloat16)
+        out = torch.empty((R, w.B, w.q_len, w.Hq, w.dv), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((R, w.B, w.Hq, w.q_len), dtype=torch.float32, device=device)
+        info = sk.sk_attn_plan_latent(w.B, w.Hq, w.q_len, w.kv_len, w.d, w.dv, w.causal, w.window_left)
+        wsb = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=device)
+
+        def call(r, st):
+            sk.sk_attn_fwd_latent(q[r], kv[r], out[r], lse[r], w.B, w.Hq, w.q_len, w.kv_len, w.d, w.dv,
+                                  w.scale, w.causal, w.window_left, wsb, wsb.numel(), st)
+
+        for i in range(warmup):
+            call(i % R, stream)
+        evb = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        eve = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        for i in range(reps):
+            flush.fill_(float(i))
+            evb[i].record(stream)
+            call(i % R, stream)
+            eve[i].record(stream)
+        torch.cuda.synchronize(device)
+        ms = statistics.median(evb[i].elapsed_time(eve[i]) for i in range(reps))
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call(0, side)
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(graph, stream=side):
+            for r in range(R):
+                call(r, side)
+        graph.replay()
+        torch.cuda.synchronize(device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(loop_reps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        loop_ms = t0.elapsed_time(t1) / (loop_reps * R)
+        del graph
+        st, where = sk.sk_attn_workspace_status(wsb)
+        if st != 0:
+            raise RuntimeError("device status %d at %d (%s)" % (st, where, w.name))
+        fl = latent_flops(w)
+        rows.append({"workload": w.name, "us": ms * 1e3, "loop_us": loop_ms * 1e3, "bytes": nbytes,
+                     "flops": fl, "splits": info.num_splits, "ctas": info.num_ctas, "kBlockM": info.kBlockM,
+                     "rotating_copies": R,
+                     "loop_tflops": fl / (loop_ms * 1e-3) / 1e12,
+                     "loop_frac_of_bf16_peak": fl / (loop_ms * 1e-3) / 1e12 / bf16_peak,
+                     "loop_frac_of_hbm_peak": nbytes / (loop_ms * 1e-3) / 1e9 / hbm_peak})
+        del q, kv, out, lse, wsb
+        torch.cuda.empty_cache()
+    return rows
+
+
+def latent_summary(rows):
+    flat = {}
+    for r in rows:
+        n = r["workload"].replace("latent_verify_", "")
+        flat[n + "_us"] = round(r["us"], 2)
+        flat[n + "_loop_us"] = round(r["loop_us"], 2)
+        flat[n + "_loop_tflops"] = round(r["loop_tflops"], 1)
+        flat[n + "_loop_frac_bf16"] = round(r["loop_frac_of_bf16_peak"], 4)
+        flat[n + "_loop_frac_hbm"] = round(r["loop_frac_of_hbm_peak"], 4)
+    return flat
+
+
 def sweep_summary(rows):
     """Flat scalars (per workload: isolated and loop microseconds and fractions
     of the HBM peak), plus the worst row of each kind."""
@@ -723,6 +834,13 @@ def main():
                       "inputs larger than 2x L2. bytes = K + V of every sequence + Q + O + LSE",
             **sweep_summary(rows)}
         result["sweep_rows"] = rows
+        lrows = gpu_latent_sweep(sk, device, hbm_peak, bf16_peak)
+        result["latent"] = {
+            "unit": "us, TFLOP/s and fractions of the bf16 and HBM peaks",
+            "method": "as the sweep; flops = 2 * (576 + 512) per visible (query, key) pair per head; "
+                      "bytes = latent rows once + Q + O + LSE",
+            **latent_summary(lrows)}
+        result["latent_rows"] = lrows
         result["host_us_per_call"] = host_cost_us(sk, device)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)

@@ -72,7 +72,8 @@ typedef enum {
 typedef enum {
     SK_PATH_AUTO = 0,
     SK_PATH_DECODE = 1,   /* <= 64 packed query rows per tile: KV rows on the MMA M axis */
-    SK_PATH_PREFILL = 2   /* 256-row tiles: two 128-row halves that share each K/V block; query rows on the MMA M axis */
+    SK_PATH_PREFILL = 2,  /* 256-row tiles: two 128-row halves that share each K/V block; query rows on the MMA M axis */
+    SK_PATH_LATENT = 3    /* latent attention (sk_attn_fwd_latent only): 16 or 32 packed rows per tile, keys on the MMA M axis */
 } sk_path;
 
 /* How the split partials are merged (sk_attn_opts.combine_mode; the stream-k
@@ -134,7 +135,7 @@ typedef struct {
     size_t workspace_bytes;   /* bytes of device workspace sk_attn_fwd needs */
     size_t echo_offset;       /* byte offset of the plan echo in the workspace */
     size_t lse_part_offset;   /* byte offset of LSE partials [S][B][Hq][q_len] fp32 */
-    size_t o_part_offset;     /* byte offset of O partials [S][B][Hq][q_len][d] fp32 */
+    size_t o_part_offset;     /* byte offset of O partials [S][B][Hq][q_len][d] fp32 (d_v wide for latent) */
     int combine_in_kernel;    /* 1: the partial kernel merges the splits itself (no second launch) */
     size_t counter_offset;    /* byte offset of the counters: per-tile arrivals (in-kernel merge) or
                                  the persistent scheduler's next-tile and finished-CTA counts */
@@ -171,6 +172,34 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
                       float scale, int causal, int window_left,
                       void* workspace, size_t ws_bytes, void* cuda_stream,
                       const sk_attn_opts* opts);
+
+/* Latent attention (absorbed multi-head latent attention, MLA): "The Occupancy
+ * Awakening", the verify attention of a speculative-decoding engine for Kimi
+ * K2.6, whose absorbed KV representation is one latent head of Dl = 512 columns
+ * plus Dr = 64 rotary columns shared by every query head.  For batch b, query
+ * head h and query row i:
+ *     s_j          = scale * <Q[b,i,h,0:576], KV[off_b+j, 0:576]>
+ *     O[b,i,h,:]   = sum_j softmax_j(s_j) KV[off_b+j, 0:512]
+ *     LSE[b,h,i]   = ln sum_j exp(s_j)
+ * over the visible keys j of row i (causal / window rules as above; the verify
+ * workload is q_len = drafts + 1 rows at the end of a prefix, causal).
+ *   - q   [B, q_len, Hq, d_qk] bf16;  kv [sum_b kv_len[b], d_qk] bf16, packed by
+ *         sequence like K above (the values are the first d_v columns of each row,
+ *         read in place);  out [B, q_len, Hq, d_v] bf16;  lse [B, Hq, q_len] fp32.
+ *   - Supported: d_qk = 576 and d_v = 512 only, any Hq >= 1; the alignment,
+ *     workspace, ownership and error rules of sk_attn_fwd.  The query heads are
+ *     packed into the tiles (PackGQA with one KV head); opts.force_path,
+ *     force_pack_gqa, combine_mode and prefill_schedule are ignored.
+ *   - The plan reports path SK_PATH_LATENT; the O partials in the workspace are
+ *     d_v wide. */
+sk_status sk_attn_plan_latent(int B, int Hq, int q_len, const int* kv_len_host, int d_qk, int d_v,
+                              int causal, int window_left, const sk_attn_opts* opts,
+                              sk_attn_plan_info* info);
+sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* lse,
+                             int B, int Hq, int q_len, const int* kv_len_host, int d_qk, int d_v,
+                             float scale, int causal, int window_left,
+                             void* workspace, size_t ws_bytes, void* cuda_stream,
+                             const sk_attn_opts* opts);
 
 /* Copy n_int32 int32 of the plan echo (written when opts.debug_echo_plan = 1;
  * same layout as sk_attn_plan_ranges) to host memory.  Synchronises cuda_stream. */

@@ -16,7 +16,8 @@ __all__ = [
     "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_status_string",
     "sk_attn_fwd_noalloc", "sk_attn_noalloc_status", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
-    "SK_PATH_PREFILL", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
+    "SK_PATH_PREFILL", "SK_PATH_LATENT", "sk_attn_plan_latent", "sk_attn_fwd_latent", "attn_fwd_latent",
+    "LATENT_DQK", "LATENT_DV", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
     "SK_SCHEDULE_ONE_TILE", "SK_SCHEDULE_PERSISTENT", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
 ]
@@ -28,7 +29,8 @@ SK_OK, SK_ERR_INVALID_ARG, SK_ERR_UNSUPPORTED, SK_ERR_WORKSPACE_TOO_SMALL = 0, 1
 SK_ERR_MISALIGNED, SK_ERR_CUDA, SK_ERR_DEVICE_TIMEOUT = 4, 5, 6
 SK_POLICY_DEFAULT, SK_POLICY_FILL, SK_POLICY_FA_HEURISTIC = 0, 1, 2
 SK_POLICY_FIXED_CHUNK, SK_POLICY_MIN_CHUNK = 3, 4
-SK_PATH_AUTO, SK_PATH_DECODE, SK_PATH_PREFILL = 0, 1, 2
+SK_PATH_AUTO, SK_PATH_DECODE, SK_PATH_PREFILL, SK_PATH_LATENT = 0, 1, 2, 3
+LATENT_DQK, LATENT_DV = 576, 512  # latent attention: 512 latent + 64 rotary key columns, 512 value columns
 SK_COMBINE_AUTO, SK_COMBINE_KERNEL, SK_COMBINE_IN_KERNEL = 0, 1, 2
 SK_SCHEDULE_AUTO, SK_SCHEDULE_ONE_TILE, SK_SCHEDULE_PERSISTENT = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 16 << 20  # SK_NOALLOC_SCRATCH_BYTES in include/sk_attn.h
@@ -94,11 +96,16 @@ def lib():
                                   vp, ctypes.POINTER(Opts)]
         L.sk_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, _intp, ci, cf, ci, ci,
                                           vp, ctypes.POINTER(Opts)]
+        L.sk_attn_plan_latent.argtypes = [ci, ci, ci, _intp, ci, ci, ci, ci, ctypes.POINTER(Opts),
+                                          ctypes.POINTER(PlanInfo)]
+        L.sk_attn_fwd_latent.argtypes = [vp, vp, vp, vp, ci, ci, ci, _intp, ci, ci, cf, ci, ci, vp, sz,
+                                         vp, ctypes.POINTER(Opts)]
         L.sk_attn_read_plan_echo.argtypes = [vp, _i32p, sz, vp]
         L.sk_attn_workspace_status.argtypes = [vp, vp, _intp]
         L.sk_attn_noalloc_status.argtypes = [vp, _intp]
         for f in ("sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd", "sk_attn_fwd_noalloc",
-                  "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_noalloc_status"):
+                  "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_noalloc_status",
+                  "sk_attn_plan_latent", "sk_attn_fwd_latent"):
             getattr(L, f).restype = ci
         L.sk_attn_status_string.argtypes = [ci]
         L.sk_attn_status_string.restype = ctypes.c_char_p
@@ -192,6 +199,28 @@ def sk_attn_fwd_noalloc(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len, d, scale, 
                                      stream, ctypes.byref(opts) if opts is not None else None))
 
 
+def sk_attn_plan_latent(B, Hq, q_len, kv_len, d_qk=LATENT_DQK, d_v=LATENT_DV, causal=False, window_left=-1,
+                        opts=None):
+    arr, _ = _kv_array(kv_len, B)
+    info = PlanInfo()
+    _check(lib().sk_attn_plan_latent(B, Hq, q_len, arr, d_qk, d_v, int(causal), int(window_left),
+                                     ctypes.byref(opts) if opts is not None else None, ctypes.byref(info)))
+    return info
+
+
+def sk_attn_fwd_latent(q, kv, out, lse, B, Hq, q_len, kv_len, d_qk, d_v, scale, causal, window_left,
+                       workspace, ws_bytes, stream=None, opts=None):
+    """Pointer-level latent attention call (one latent KV head; the values are
+    the first d_v columns of each kv row)."""
+    arr, _ = _kv_array(kv_len, B)
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _check(lib().sk_attn_fwd_latent(_ptr(q), _ptr(kv), _ptr(out), _ptr(lse), B, Hq, q_len, arr, d_qk, d_v,
+                                    float(scale), int(causal), int(window_left), _ptr(workspace),
+                                    int(ws_bytes), stream,
+                                    ctypes.byref(opts) if opts is not None else None))
+
+
 def sk_attn_noalloc_status(stream=None):
     """Status word left by the last sk_attn_fwd_noalloc call on the current
     device: returns (status, where) like sk_attn_workspace_status."""
@@ -255,4 +284,42 @@ def attn_fwd(q, k, v, kv_len, scale=None, causal=False, window_left=-1, out=None
         stream = torch.cuda.current_stream(q.device)
     sk_attn_fwd(q, k, v, out, lse, B, Hq, Hkv, sq, kv_len, d, scale, causal, window_left,
                 workspace, workspace.numel(), stream, opts)
+    return out, lse, workspace
+
+
+def attn_fwd_latent(q, kv, kv_len, scale=None, causal=False, window_left=-1, out=None, lse=None,
+                    workspace=None, opts=None, stream=None):
+    """Convenience wrapper over sk_attn_fwd_latent for torch CUDA tensors.
+
+    q [B, q_len, Hq, 576], kv [sum(kv_len), 576] (bf16, contiguous): one latent
+    head whose rows are the keys and whose first 512 columns are the values.
+    Allocates out [B, q_len, Hq, 512] bf16, lse [B, Hq, q_len] fp32 and a
+    zeroed workspace when they are not given.  Returns (out, lse, workspace).
+    """
+    import torch
+    if q.dtype != torch.bfloat16 or kv.dtype != torch.bfloat16:
+        raise TypeError("q and kv must be bfloat16")
+    if not (q.is_cuda and kv.is_cuda):
+        raise TypeError("q and kv must be CUDA tensors")
+    if not (q.is_contiguous() and kv.is_contiguous()):
+        raise ValueError("q and kv must be contiguous")
+    B, sq, Hq, d = q.shape
+    T, d2 = kv.shape
+    kv_len = [int(x) for x in kv_len]
+    if d != LATENT_DQK or d2 != d or len(kv_len) != B or sum(kv_len) != T:
+        raise ValueError("shape mismatch between q, kv and kv_len (q [B, q_len, Hq, 576], kv [sum(kv_len), 576])")
+    if scale is None:
+        scale = 1.0 / float(d) ** 0.5
+    info = sk_attn_plan_latent(B, Hq, sq, kv_len, LATENT_DQK, LATENT_DV, causal, window_left, opts)
+    if out is None:
+        out = torch.empty((B, sq, Hq, LATENT_DV), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, sq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.zeros(max(int(info.workspace_bytes), 256), dtype=torch.uint8,
+                                device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sk_attn_fwd_latent(q, kv, out, lse, B, Hq, sq, kv_len, LATENT_DQK, LATENT_DV, scale, causal, window_left,
+                       workspace, workspace.numel(), stream, opts)
     return out, lse, workspace

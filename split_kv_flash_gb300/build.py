@@ -14,7 +14,8 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["api.cu", "fwd_decode.cu", "fwd_prefill.cu", "fwd_prefill_persistent.cu", "combine.cu", "noalloc.cu"]
+CU_SOURCES = ["api.cu", "fwd_decode.cu", "fwd_prefill.cu", "fwd_prefill_persistent.cu", "fwd_latent.cu", "combine.cu",
+              "noalloc.cu"]
 CXX_SOURCES = ["plan.cpp"]
 
 

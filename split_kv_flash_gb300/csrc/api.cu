@@ -1,6 +1,6 @@
 // api.cu -- the C ABI declared in include/sk_attn.h: argument checks, the host
 // plan, TMA tensor maps for K and V, and the launches of the partial kernel and
-// the combine kernel on the caller's stream.
+// the combine kernel on the caller's stream (standard and latent attention).
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <string.h>
@@ -126,7 +126,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // ---- per-thread cache of plans and tensor maps
 struct CallKey {
-    int dev, B, Hq, Hkv, q_len, d, causal, window_left;
+    int dev, B, Hq, Hkv, q_len, d, dv, latent, causal, window_left;
     int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms, combine_mode, prefill_schedule;
     const void *q, *k, *v, *out;
 };
@@ -241,11 +241,15 @@ sk_status sk_attn_plan_ranges(int B, int Hq, int Hkv, int q_len, const int* kv_l
     return SK_OK;
 }
 
-sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
-                      int Hkv, int q_len, const int* kv_len_host, int d, float scale, int causal,
-                      int window_left, void* workspace, size_t ws_bytes, void* cuda_stream,
-                      const sk_attn_opts* opts) {
-    g_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// Both forward entry points.  Latent attention: one KV head (Hkv = 1) of width
+// d whose rows are the keys and whose first dv columns are the values (k == v).
+sk_status fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                   int q_len, const int* kv_len_host, int d, int dv, bool latent, float scale, int causal,
+                   int window_left, void* workspace, size_t ws_bytes, void* cuda_stream, const sk_attn_opts* opts) {
     sk_attn_opts o;
     memset(&o, 0, sizeof o);
     if (opts) o = *opts;
@@ -261,6 +265,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     CallKey key;
     memset(&key, 0, sizeof key);
     key.dev = di.dev; key.B = B; key.Hq = Hq; key.Hkv = Hkv; key.q_len = q_len; key.d = d;
+    key.dv = dv; key.latent = latent ? 1 : 0;
     key.causal = causal ? 1 : 0; key.window_left = window_left < 0 ? -1 : window_left;
     key.policy = o.policy; key.force_num_splits = o.force_num_splits; key.force_pack_gqa = o.force_pack_gqa;
     key.force_path = o.force_path; key.max_splits = o.max_splits; key.num_sms = o.num_sms;
@@ -271,7 +276,10 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     if (!ce) {
         CallEntry fresh;
         std::string why;
-        s = make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, &o, di.sms, &fresh.plan, &why);
+        s = latent ? make_plan_latent(B, Hq, q_len, kv_len_host, d, dv, causal, window_left, &o, di.sms,
+                                      &fresh.plan, &why)
+                   : make_plan(B, Hq, Hkv, q_len, kv_len_host, d, causal, window_left, &o, di.sms, &fresh.plan,
+                               &why);
         if (s != SK_OK) return fail(s, why);
         const Plan& p = fresh.plan;
         if (p.num_ctas == 0) return SK_OK;  // q_len == 0: nothing to compute
@@ -329,7 +337,7 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     fp.fused_combine = p.fused_combine ? 1 : 0;
 
     fp.status = reinterpret_cast<uint32_t*>(ws);
-    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.G = p.G; fp.sq = q_len; fp.d = d;
+    fp.B = B; fp.Hq = Hq; fp.Hkv = p.Hkv; fp.G = p.G; fp.sq = q_len; fp.d = d;
     fp.pack_gqa = p.pack_gqa ? 1 : 0;
     fp.rows = p.rows;
     fp.kBlockM = p.kBlockM; fp.kBlockN = p.kBlockN;
@@ -350,7 +358,9 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     cudaError_t e;
     if (o.event_begin && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_begin), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
-    if (p.path == SK_PATH_DECODE)
+    if (p.path == SK_PATH_LATENT)
+        e = launch_latent(p, fp, tmK, stream);
+    else if (p.path == SK_PATH_DECODE)
         e = launch_decode(p, fp, tmK, tmV, stream);
     else if (p.persistent && q_tma)
         e = launch_prefill_persistent(p, fp, tmK, tmV, tmQ, stream);
@@ -364,6 +374,46 @@ sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
         if (e != cudaSuccess) return fail_cuda(e, "combine kernel launch");
     }
     return SK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sk_status sk_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                      int Hkv, int q_len, const int* kv_len_host, int d, float scale, int causal,
+                      int window_left, void* workspace, size_t ws_bytes, void* cuda_stream,
+                      const sk_attn_opts* opts) {
+    g_last_error.clear();
+    return fwd_impl(q, k, v, out, lse, B, Hq, Hkv, q_len, kv_len_host, d, d, false, scale, causal, window_left,
+                    workspace, ws_bytes, cuda_stream, opts);
+}
+
+sk_status sk_attn_plan_latent(int B, int Hq, int q_len, const int* kv_len_host, int d_qk, int d_v, int causal,
+                              int window_left, const sk_attn_opts* opts, sk_attn_plan_info* info) {
+    g_last_error.clear();
+    if (!info) return fail(SK_ERR_INVALID_ARG, "info is NULL");
+    int sms = 0;
+    if (!opts || opts->num_sms <= 0) {
+        DeviceInfo di;
+        sk_status s = current_device(&di);
+        if (s != SK_OK) return s;
+        sms = di.sms;
+    }
+    Plan p;
+    std::string why;
+    sk_status s = make_plan_latent(B, Hq, q_len, kv_len_host, d_qk, d_v, causal, window_left, opts, sms, &p, &why);
+    if (s != SK_OK) return fail(s, why);
+    plan_to_info(p, info);
+    return SK_OK;
+}
+
+sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* lse, int B, int Hq, int q_len,
+                             const int* kv_len_host, int d_qk, int d_v, float scale, int causal, int window_left,
+                             void* workspace, size_t ws_bytes, void* cuda_stream, const sk_attn_opts* opts) {
+    g_last_error.clear();
+    return fwd_impl(q, kv, kv, out, lse, B, Hq, 1, q_len, kv_len_host, d_qk, d_v, true, scale, causal,
+                    window_left, workspace, ws_bytes, cuda_stream, opts);
 }
 
 sk_status sk_attn_read_plan_echo(const void* workspace, int32_t* ranges_host, size_t n_int32, void* cuda_stream) {

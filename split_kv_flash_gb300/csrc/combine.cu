@@ -15,7 +15,9 @@
 //    in flight at once and the merge costs about one L2 round trip;
 //  - few splits (S <= 16; verify, batched decode: many rows, few splits): one
 //    warp per row, 8 rows per CTA, lane s holding split s's LSE and lane c the
-//    float4 columns c of the row, so a CTA is not launched for a few loads.
+//    float4 columns c, c + 32, ... of the row, so a CTA is not launched for a
+//    few loads.
+// Rows are 64, 128 or 512 values wide (512: latent attention).
 // Both are launched as programmatic dependents of the partial kernel: they are
 // scheduled while the partial kernel runs and wait (griddepcontrol.wait) for
 // that grid's completion and memory before they read anything.
@@ -33,9 +35,10 @@ constexpr float kLog2e = 1.4426950408889634074f;
 template <int HD, class Seqs>
 __global__ void __launch_bounds__(32 * kWarps)
     combine_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ Seqs seqs) {
-    constexpr int kCols4 = HD / 4;       // float4 columns of a row: 32 (d=128) or 16 (d=64)
-    __shared__ float w_s[kMaxSplits];    // merge weight of each split
-    __shared__ float4 part[kWarps][32];  // per-warp partial sums
+    constexpr int kCols4 = HD / 4;          // float4 columns of a row: 16, 32 or 128
+    constexpr int kPer = (kCols4 + 31) / 32;  // per lane
+    __shared__ float w_s[kMaxSplits];       // merge weight of each split
+    __shared__ float4 part[kWarps][32 * kPer];  // per-warp partial sums
     __shared__ float lse_row;
 
     const int warp = threadIdx.x >> 5;
@@ -80,35 +83,40 @@ __global__ void __launch_bounds__(32 * kWarps)
     }
     __syncthreads();
 
-    // 2. weighted sum of the O partials, splits spread over the warps.
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < kCols4) {
-        const float4* src = reinterpret_cast<const float4*>(p.o_part + base * HD) + lane;
-        const size_t stride4 = stride * (HD / 4);
-        constexpr int kUnroll = kMaxSplits / kWarps;  // 16
-        float4 v[kUnroll];
+    // 2. weighted sum of the O partials, splits spread over the warps; lane c
+    //    holds float4 columns c, c + 32, ... of the row.
+    const float4* src0 = reinterpret_cast<const float4*>(p.o_part + base * HD);
+    const size_t stride4 = stride * (HD / 4);
+#pragma unroll 1
+    for (int t = 0; t < kPer; ++t) {
+        const int c = t * 32 + lane;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < kCols4) {
+            constexpr int kUnroll = kMaxSplits / kWarps;  // 16
+            float4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int s = warp + u * kWarps;
-            v[u] = (s < S) ? __ldcg(src + s * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+            for (int u = 0; u < kUnroll; ++u) {
+                const int s = warp + u * kWarps;
+                v[u] = (s < S) ? __ldcg(src0 + c + s * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int s = warp + u * kWarps;
-            const float ws = (s < S) ? w_s[s] : 0.f;
-            acc.x += ws * v[u].x;
-            acc.y += ws * v[u].y;
-            acc.z += ws * v[u].z;
-            acc.w += ws * v[u].w;
+            for (int u = 0; u < kUnroll; ++u) {
+                const int s = warp + u * kWarps;
+                const float ws = (s < S) ? w_s[s] : 0.f;
+                acc.x += ws * v[u].x;
+                acc.y += ws * v[u].y;
+                acc.z += ws * v[u].z;
+                acc.w += ws * v[u].w;
+            }
         }
+        part[warp][c] = acc;
     }
-    part[warp][lane] = acc;
     __syncthreads();
-    if (warp == 0 && lane < kCols4) {
-        float4 t = part[0][lane];
+    for (int c = threadIdx.x; c < kCols4; c += 32 * kWarps) {
+        float4 t = part[0][c];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) {
-            const float4 u = part[w][lane];
+            const float4 u = part[w][c];
             t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
         }
         uint2 packed;
@@ -116,9 +124,9 @@ __global__ void __launch_bounds__(32 * kWarps)
         __nv_bfloat162 hi = __floats2bfloat162_rn(t.z, t.w);
         packed.x = *reinterpret_cast<uint32_t*>(&lo);
         packed.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.sq + i) * p.Hq + h) * HD + lane * 4) = packed;
-        if (lane == 0) p.lse[base] = lse_row;
+        *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.sq + i) * p.Hq + h) * HD + c * 4) = packed;
     }
+    if (threadIdx.x == 0) p.lse[base] = lse_row;
 }
 
 constexpr int kRowsMaxSplits = 16;  // the warp-per-row shape handles up to this many splits
@@ -127,6 +135,7 @@ template <int HD, class Seqs>
 __global__ void __launch_bounds__(32 * kWarps)
     combine_rows_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ Seqs seqs, long long rows) {
     constexpr int kCols4 = HD / 4;
+    constexpr int kPer = (kCols4 + 31) / 32;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * kWarps + warp;
@@ -153,28 +162,37 @@ __global__ void __launch_bounds__(32 * kWarps)
     const float lse = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
     const float w = (l == -INFINITY || lse == -INFINITY) ? 0.f : exp2f((l - lse) * kLog2e);
 
-    // weighted sum of the O partials: lane c holds float4 column c
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // weighted sum of the O partials: lane c holds float4 columns c, c + 32, ...
+    float4 acc[kPer];
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* src = reinterpret_cast<const float4*>(p.o_part + base * HD) + lane;
     const size_t stride4 = stride * (HD / 4);
 #pragma unroll 4
     for (int s = 0; s < S; ++s) {
         const float ws = __shfl_sync(0xffffffffu, w, s);
-        if (lane < kCols4) {
-            const float4 v = __ldcg(src + s * stride4);
-            acc.x += ws * v.x;
-            acc.y += ws * v.y;
-            acc.z += ws * v.z;
-            acc.w += ws * v.w;
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {
+            if (t * 32 + lane < kCols4) {
+                const float4 v = __ldcg(src + t * 32 + s * stride4);
+                acc[t].x += ws * v.x;
+                acc[t].y += ws * v.y;
+                acc[t].z += ws * v.z;
+                acc[t].w += ws * v.w;
+            }
         }
     }
-    if (lane < kCols4) {
-        uint2 packed;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        packed.x = *reinterpret_cast<uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.sq + i) * p.Hq + h) * HD + lane * 4) = packed;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+        const int c = t * 32 + lane;
+        if (c < kCols4) {
+            uint2 packed;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[t].x, acc[t].y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[t].z, acc[t].w);
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(p.out + (((size_t)b * p.sq + i) * p.Hq + h) * HD + c * 4) = packed;
+        }
     }
     if (lane == 0) p.lse[base] = lse;
 }
@@ -203,15 +221,25 @@ cudaError_t launch_c(const Plan& plan, const FwdParams& p, const Seqs& seqs, cud
 
 }  // namespace
 
+template <class Seqs>
+cudaError_t launch_width(const Plan& plan, const FwdParams& p, const Seqs& seqs, cudaStream_t stream) {
+    switch (plan.dv) {
+        case 64: return launch_c<64>(plan, p, seqs, stream);
+        case 128: return launch_c<128>(plan, p, seqs, stream);
+        case 512: return launch_c<512>(plan, p, seqs, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream) {
     if (plan.num_splits > kMaxSplits) return cudaErrorInvalidValue;
     if (!plan.varlen) {
         UniformSeqs u{plan.kv_len[0], plan.splits_b[0]};
-        return plan.d == 128 ? launch_c<128>(plan, p, u, stream) : launch_c<64>(plan, p, u, stream);
+        return launch_width(plan, p, u, stream);
     }
     VarlenSeqs v;
     fill_varlen(plan, &v);
-    return plan.d == 128 ? launch_c<128>(plan, p, v, stream) : launch_c<64>(plan, p, v, stream);
+    return launch_width(plan, p, v, stream);
 }
 
 }  // namespace sk

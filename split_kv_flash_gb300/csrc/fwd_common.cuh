@@ -97,6 +97,7 @@ cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorM
                            cudaStream_t stream);
 cudaError_t launch_prefill_persistent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, const CUtensorMap& tmQ, cudaStream_t stream);
+cudaError_t launch_latent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmKV, cudaStream_t stream);
 cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 
 void fill_varlen(const Plan& plan, VarlenSeqs* v);

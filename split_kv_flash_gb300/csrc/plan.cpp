@@ -99,9 +99,30 @@ int fill_policy(const Plan& p, int capacity, int max_splits) {
 
 }  // namespace
 
+namespace {
+sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int dv, bool latent,
+                       int causal, int window_left, const sk_attn_opts* opts_in, int device_num_sms, Plan* out,
+                       std::string* why);
+}  // namespace
+
 sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int causal,
-                    int window_left, const sk_attn_opts* opts_in, int device_num_sms, Plan* out,
+                    int window_left, const sk_attn_opts* opts, int device_num_sms, Plan* out,
                     std::string* why) {
+    return make_plan_ex(B, Hq, Hkv, q_len, kv_len_host, d, d, false, causal, window_left, opts, device_num_sms,
+                        out, why);
+}
+
+sk_status make_plan_latent(int B, int Hq, int q_len, const int* kv_len_host, int d, int dv, int causal,
+                           int window_left, const sk_attn_opts* opts, int device_num_sms, Plan* out,
+                           std::string* why) {
+    return make_plan_ex(B, Hq, 1, q_len, kv_len_host, d, dv, true, causal, window_left, opts, device_num_sms,
+                        out, why);
+}
+
+namespace {
+sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int dv, bool latent,
+                       int causal, int window_left, const sk_attn_opts* opts_in, int device_num_sms, Plan* out,
+                       std::string* why) {
     sk_attn_opts opts;
     memset(&opts, 0, sizeof opts);
     if (opts_in) opts = *opts_in;
@@ -115,7 +136,12 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     if (Hq % Hkv != 0) return fail(SK_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
     if (q_len < 0 || q_len > kMaxSeqLen) return fail(SK_ERR_INVALID_ARG, "q_len out of range");
     if (!kv_len_host) return fail(SK_ERR_INVALID_ARG, "kv_len_host is NULL");
-    if (d != 64 && d != 128) return fail(SK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (latent) {
+        if (d != kLatentDqk || dv != kLatentDv)
+            return fail(SK_ERR_UNSUPPORTED, "latent attention: key width 576 and value width 512 only");
+    } else if (d != 64 && d != 128) {
+        return fail(SK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    }
     if (opts.policy < 0 || opts.policy > SK_POLICY_MIN_CHUNK)
         return fail(SK_ERR_INVALID_ARG, "unknown split policy");
     if (opts.force_path < 0 || opts.force_path > SK_PATH_PREFILL)
@@ -131,6 +157,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
         return fail(SK_ERR_INVALID_ARG, "unknown prefill schedule");
 
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.sq = q_len; p.d = d;
+    p.dv = dv;
+    p.latent = latent;
     p.causal = causal ? 1 : 0;
     p.window_left = window_left < 0 ? -1 : window_left;
     p.win = key_window(p.causal, p.window_left);
@@ -157,6 +185,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     bool pack = should_pack_gqa(false, q_len, p.G, 128);
     if (opts.force_pack_gqa == 1) pack = true;
     if (opts.force_pack_gqa == -1) pack = false;
+    if (latent) pack = true;  // every query head reads the one latent head
     if (p.G == 1) pack = false;
     p.pack_gqa = pack;
     p.head_tiles = pack ? Hkv : Hq;
@@ -165,13 +194,15 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     p.rows = int(rows);
 
     // Kernel choice: at most 64 packed rows -> decode kernel (KV rows on MMA M).
-    int path = opts.force_path;
+    int path = latent ? int(SK_PATH_LATENT) : opts.force_path;
     if (path == SK_PATH_AUTO) path = (p.rows <= kDecodeMaxRows) ? SK_PATH_DECODE : SK_PATH_PREFILL;
     if (path == SK_PATH_DECODE && p.rows > kDecodeMaxRows)
         return fail(SK_ERR_UNSUPPORTED, "decode path holds at most 64 packed rows per tile");
     p.path = path;
     p.kBlockN = 128;
-    if (path == SK_PATH_DECODE) {
+    if (path == SK_PATH_LATENT) {
+        p.kBlockM = p.rows <= 16 ? 16 : 32;  // packed rows per tile; keys on the MMA M axis
+    } else if (path == SK_PATH_DECODE) {
         p.kBlockM = std::max(16, (p.rows + 15) / 16 * 16);
     } else {
         // Prefill kernel: 256-row tiles, two 128-row halves that share each K/V block.
@@ -192,7 +223,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     } else {
         switch (opts.policy) {
             case SK_POLICY_FA_HEURISTIC: {
-                const long long kv_head_bytes = (long long)p.max_kv * (2LL * d) * 2;
+                const long long kv_head_bytes = (long long)p.max_kv * (d + dv) * 2;
                 S = num_splits_fa_heuristic(int(std::min<long long>(tiles, 1LL << 30)), p.num_sms,
                                             p.nblk_max, p.num_m_blocks, kv_head_bytes,
                                             p.causal || p.window_left >= 0, max_splits);
@@ -232,14 +263,14 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     {
         const int gp = p.pack_gqa ? p.G : 1;
         const long long tiles = (long long)p.num_m_blocks * p.head_tiles * p.num_splits * B;
-        p.persistent = p.path == SK_PATH_PREFILL && opts.prefill_schedule == SK_SCHEDULE_PERSISTENT &&
+        p.persistent = !latent && p.path == SK_PATH_PREFILL && opts.prefill_schedule == SK_SCHEDULE_PERSISTENT &&
                        128 % gp == 0 && (long long)B * q_len < (1LL << 31) && tiles > 0 && tiles < (1LL << 30);
         if (p.persistent) {
             p.persistent_ctas = int(std::min<long long>(tiles, p.num_sms));
             // Section 4.4: nearest_power_of_2(32 MB / size of one KV head) heads,
             // times the query heads per KV head when those are separate tiles
             // (power of two taken downwards, so that a section fits the budget).
-            const long long kv_head_bytes = std::max<long long>(1, (long long)p.max_kv * (2LL * d) * 2);
+            const long long kv_head_bytes = std::max<long long>(1, (long long)p.max_kv * (d + dv) * 2);
             long long per = (32LL << 20) / kv_head_bytes;
             long long pow2 = 1;
             while (pow2 * 2 <= per) pow2 *= 2;
@@ -266,7 +297,7 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
         const size_t rows_all = size_t(p.num_splits) * B * Hq * size_t(q_len);
         off = align_up(off + rows_all * 4, 256);
         p.o_off = off;
-        off = align_up(off + rows_all * size_t(d) * 4, 256);
+        off = align_up(off + rows_all * size_t(dv) * 4, 256);
     } else {
         p.o_off = off;
     }
@@ -274,6 +305,8 @@ sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, i
     *out = std::move(p);
     return SK_OK;
 }
+
+}  // namespace
 
 void plan_ranges(const Plan& p, int32_t* out) {
     long long idx = 0;

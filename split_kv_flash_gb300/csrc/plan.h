@@ -27,6 +27,8 @@ constexpr int decode_ring_bytes(int hd, int np) {
 struct Plan {
     // problem
     int B = 0, Hq = 0, Hkv = 0, G = 1, sq = 0, d = 0;
+    int dv = 0;           // value / output width (= d except for latent attention)
+    bool latent = false;  // one latent KV head: keys are its rows, values their first dv columns
     int causal = 0, window_left = -1;
     KeyWindow win{};
     bool varlen = false;       // kv lengths differ between sequences
@@ -58,6 +60,13 @@ struct Plan {
 sk_status make_plan(int B, int Hq, int Hkv, int q_len, const int* kv_len_host, int d, int causal,
                     int window_left, const sk_attn_opts* opts, int device_num_sms, Plan* plan,
                     std::string* why);
+// Latent attention (one KV head whose rows are the keys and whose first dv
+// columns are the values; "The Occupancy Awakening", absorbed-MLA verify).
+sk_status make_plan_latent(int B, int Hq, int q_len, const int* kv_len_host, int d, int dv, int causal,
+                           int window_left, const sk_attn_opts* opts, int device_num_sms, Plan* plan,
+                           std::string* why);
+constexpr int kLatentDqk = 576;  // 512 latent + 64 rotary columns
+constexpr int kLatentDv = 512;
 
 // Host-side range table (see sk_attn_plan_ranges).
 void plan_ranges(const Plan& p, int32_t* out);

@@ -168,3 +168,42 @@ def test_persistent_prefill_plan(sk):
     assert sk.sk_attn_plan(1, 32, 4, 1, [4096], 128, opts=o).persistent == 0  # decode path
     with pytest.raises(sk.SKError):
         sk.sk_attn_plan(1, 2, 2, 300, [300], 128, True, opts=_opts(sk, prefill_schedule=7))
+
+
+def test_latent_plan(sk):
+    """Latent attention plans: the latent path, every query head packed into
+    16- or 32-row tiles of the one latent head, partials 512 columns wide;
+    other widths are refused."""
+    o = _opts(sk, num_sms=152)
+    info = sk.sk_attn_plan_latent(2, 64, 9, [521, 521], 576, 512, True, opts=o)
+    assert info.path == sk.SK_PATH_LATENT
+    assert info.pack_gqa == 1 and info.head_tiles == 1
+    assert info.rows_per_head_tile == 9 * 64 and info.kBlockM == 32
+    assert info.num_m_blocks == 18
+    assert info.grid_x == 18 and info.grid_y == info.num_splits and info.grid_z == 2
+    if info.needs_combine:
+        rows = info.num_splits * 2 * 64 * 9
+        assert info.o_part_offset - info.lse_part_offset >= rows * 4
+        assert info.workspace_bytes - info.o_part_offset >= rows * 512 * 4
+    assert sk.sk_attn_plan_latent(1, 8, 2, [4096], opts=o).kBlockM == 16
+    # one query head: nothing to pack, one head tile of q_len rows
+    one = sk.sk_attn_plan_latent(1, 1, 5, [300], opts=o)
+    assert one.pack_gqa == 0 and one.rows_per_head_tile == 5 and one.path == sk.SK_PATH_LATENT
+    for d_qk, d_v in ((128, 128), (576, 576), (512, 512), (576, 128)):
+        with pytest.raises(sk.SKError) as ei:
+            sk.sk_attn_plan_latent(1, 16, 2, [100], d_qk, d_v, opts=o)
+        assert ei.value.status == 2
+    # the standard entry point does not accept the latent path or width
+    with pytest.raises(sk.SKError):
+        sk.sk_attn_plan(1, 16, 1, 2, [100], 576, opts=o)
+    with pytest.raises(sk.SKError):
+        sk.sk_attn_plan(1, 16, 1, 2, [100], 128, opts=_opts(sk, num_sms=152, force_path=3))
+
+
+def test_latent_fwd_without_gpu_fails_cleanly(sk):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_attn_fwd_latent(16, 16, 16, 16, 1, 16, 2, [256], 576, 512, 0.07, 1, -1, 256, 1 << 20)
+    assert ei.value.status in (2, 5)

@@ -13,6 +13,11 @@ bf16 bits go to the GPU and, as uint16 bit patterns, to the oracle.
 Layouts: Q [B, sq, Hq, d]; K, V [sum_b kv_len[b], Hkv, d] packed by sequence
 (sequence b starts at the sum of the lengths before it); O [B, sq, Hq, d];
 LSE [B, Hq, sq].
+
+Latent workloads (one latent KV head of 576 columns shared by all query heads):
+the generator draws Q [B, sq, Hq, 576] then KV [sum_b kv_len[b], 576] as float32
+standard normals rounded to bf16, and multiplies the bf16 KV by kv_scale (0.5 by
+default, exact); the values are the first 512 columns of KV.
 """
 from dataclasses import dataclass, field
 from typing import List, Optional
@@ -107,3 +112,48 @@ def prefill(local: bool, seqlen: int = 8192, B: int = 4) -> Workload:
     return Workload("prefill_b%d_hq32_hkv8_d128_s%d_%s" % (B, seqlen, "local1024" if local else "causal"),
                     B, 32, 8, 128, seqlen, [seqlen] * B, causal=True,
                     window_left=1024 if local else -1, seed=1400 + (1 if local else 0))
+
+
+@dataclass
+class LatentWorkload:
+    """Absorbed-MLA verify: one latent head (512 latent + 64 rotary columns)."""
+    name: str
+    B: int
+    Hq: int
+    q_len: int
+    kv_len: List[int]
+    causal: bool = True
+    window_left: int = -1
+    seed: int = 0
+    kv_scale: float = 0.5
+    d: int = 576
+    dv: int = 512
+
+    @property
+    def scale(self) -> float:
+        # The model's query-key width before absorption: 128 non-rotary + 64
+        # rotary columns per head.
+        return 1.0 / float(np.sqrt(192.0))
+
+    @property
+    def total_kv(self) -> int:
+        return int(sum(self.kv_len))
+
+
+def make_latent_inputs(w: LatentWorkload):
+    """Return (q, kv) as CPU bf16 tensors for latent workload w."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.B, w.q_len, w.Hq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    kv = torch.randn((w.total_kv, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    if w.kv_scale != 1.0:
+        kv = kv * w.kv_scale
+    return q, kv
+
+
+def latent_verify(B: int, Hq: int, q_len: int, kv_len, causal: bool = True, seed: int = 1500) -> LatentWorkload:
+    """Latent-attention speculative verify (Kimi K2.6 shapes of "The Occupancy
+    Awakening"): q_len = drafts + 1 query rows at the end of the sequence."""
+    kv = [int(x) for x in (kv_len if isinstance(kv_len, (list, tuple)) else [kv_len] * B)]
+    return LatentWorkload("latent_verify_b%d_h%d_q%d_kv%s%s" % (B, Hq, q_len, "-".join(map(str, sorted(set(kv)))),
+                                                             "" if causal else "_nomask"),
+                          B, Hq, q_len, kv, causal=causal, seed=seed)

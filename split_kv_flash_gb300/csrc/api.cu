@@ -58,6 +58,25 @@ bool make_kv_map(CUtensorMap* m, const void* base, int Hkv, int d, long long row
     return r == CUDA_SUCCESS;
 }
 
+// Latent rows [rows][576] as a 3-D bf16 tensor (64 columns, rows, 9 column
+// chunks): the chunk dimension has a 128-byte stride, so a box of
+// (64, 128, z) is z consecutive 64-column chunks of 128 rows, laid out in
+// shared memory chunk after chunk, each [128 rows][128 bytes] with the
+// 128-byte swizzle.  One copy then moves z x 16 KB (larger copies stream
+// faster than 16 KB ones).
+bool make_latent_map(CUtensorMap* m, const void* base, long long rows, int z, int box_rows = 128) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, cuuint64_t(rows), cuuint64_t(kLatentDqk / 64)};
+    cuuint64_t strides[2] = {cuuint64_t(kLatentDqk) * 2, 128};
+    cuuint32_t box[3] = {64, cuuint32_t(box_rows), cuuint32_t(z)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Q [B * q_len][Hq][d] as a 4-D bf16 tensor (d, gp, Hq / gp, B * q_len): a box
 // of (64, gp, 1, 128 / gp) is 128 rows of 128 bytes in packed-row order
 // (query position major, the gp query heads of a group minor), 128-byte
@@ -294,8 +313,14 @@ sk_status fwd_impl(const void* q, const void* k, const void* v, void* out, float
         const void* kb = total_kv > 0 ? k : out;
         const void* vb = total_kv > 0 ? v : out;
         const long long rows = total_kv > 0 ? total_kv : 1;
-        if (!make_kv_map(&fresh.tmK, kb, Hkv, d, rows) || !make_kv_map(&fresh.tmV, vb, Hkv, d, rows))
+        if (latent) {
+            // K: three 64-column chunks per copy; V: one 128-column group per copy.
+            if (!make_latent_map(&fresh.tmK, kb, rows, kLatentKChunksPerCopy) ||
+                !make_latent_map(&fresh.tmV, vb, rows, 2))
+                return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (latent)");
+        } else if (!make_kv_map(&fresh.tmK, kb, Hkv, d, rows) || !make_kv_map(&fresh.tmV, vb, Hkv, d, rows)) {
             return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        }
         // Prefill tiles take Q by TMA when a 128-row half is whole row groups of
         // the map (128 % gp == 0) and every row index fits the copy's int32
         // coordinate.  Final prefill outputs (one split per sequence) leave
@@ -307,6 +332,15 @@ sk_status fwd_impl(const void* q, const void* k, const void* v, void* out, float
         fresh.q_tma = p.path == SK_PATH_PREFILL && 128 % fresh.q_gp == 0 && q_rows < (1LL << 31);
         if (fresh.q_tma && !make_q_map(&fresh.tmQ, q, q_rows, Hq, d, fresh.q_gp))
             return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (Q)");
+        if (latent) {
+            // Q rows [B * q_len * Hq][576]: a tile's packed rows are consecutive
+            // rows of this tensor, so its Q^T arrives as three boxes of
+            // (64, kBlockM, 3).
+            const long long rows_q = (long long)B * q_len * Hq;
+            if (rows_q >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "latent: B * q_len * Hq must be < 2^31");
+            if (!make_latent_map(&fresh.tmQ, q, rows_q, 3, p.kBlockM))
+                return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (latent Q)");
+        }
         fresh.o_tma = fresh.q_tma && !p.needs_combine && !p.persistent;
         if (fresh.o_tma && !make_o_map(&fresh.tmO, out, B, q_len, Hq, d, fresh.q_gp))
             return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (O)");
@@ -359,7 +393,7 @@ sk_status fwd_impl(const void* q, const void* k, const void* v, void* out, float
     if (o.event_begin && (e = cudaEventRecord(static_cast<cudaEvent_t>(o.event_begin), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
     if (p.path == SK_PATH_LATENT)
-        e = launch_latent(p, fp, tmK, stream);
+        e = launch_latent(p, fp, tmK, tmV, tmQ, stream);
     else if (p.path == SK_PATH_DECODE)
         e = launch_decode(p, fp, tmK, tmV, stream);
     else if (p.persistent && q_tma)

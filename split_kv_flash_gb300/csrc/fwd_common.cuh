@@ -97,7 +97,11 @@ cudaError_t launch_prefill(const Plan& plan, const FwdParams& p, const CUtensorM
                            cudaStream_t stream);
 cudaError_t launch_prefill_persistent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, const CUtensorMap& tmQ, cudaStream_t stream);
-cudaError_t launch_latent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmKV, cudaStream_t stream);
+// tmK: latent rows as 3-D boxes of kLatentKChunksPerCopy 64-column chunks;
+// tmV: the same rows as boxes of 2 chunks (one 128-column value group);
+// tmQ: query rows as boxes of (64 columns, kBlockM rows, 3 chunks).
+cudaError_t launch_latent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap& tmQ, cudaStream_t stream);
 cudaError_t launch_combine(const Plan& plan, const FwdParams& p, cudaStream_t stream);
 
 void fill_varlen(const Plan& plan, VarlenSeqs* v);

@@ -15,9 +15,9 @@
 // read of a row hits L2).  Online softmax, masks, split epilogue and bounded
 // waits are those of the decode kernel (fwd_decode.cu).
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 2-5 softmax (thread t <-> TMEM lane t = key t of S^T and value
-// column t of each O_g^T) and epilogue.
+// Warp roles (224 threads): warp 0 TMA producer of K chunks, warp 6 of V
+// groups, warp 1 TMEM owner and MMA issuer, warps 2-5 softmax (thread t <->
+// TMEM lane t = key t of S^T and value column t of each O_g^T) and epilogue.
 #include <math.h>
 
 #include "fwd_common.cuh"
@@ -27,13 +27,14 @@
 namespace sk {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kDq = kLatentDqk;        // 576
 constexpr int kDv = kLatentDv;         // 512
 constexpr int kQChunks = kDq / 64;     // 9
 constexpr int kVGroups = kDv / 128;    // 4
+static_assert(kQChunks % kLatentKChunksPerCopy == 0, "K copies cover whole blocks");
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -51,19 +52,36 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Ring depths per tile height (K slots of kLatentKChunksPerCopy chunks, V
+// groups, P^T buffers): what the shared memory left after Q^T (9 x NP x 128
+// bytes) holds.
+template <int NP>
+struct LatentRings;
+template <>
+struct LatentRings<16> {
+    static constexpr int k = 2, v = 3, p = 2;
+};
+template <>
+struct LatentRings<32> {
+    static constexpr int k = 2, v = 2, p = 2;
+};
+
 template <int NP>
 struct LatentCfg {
-    static constexpr int kStagesK = 6;                 // 64-column K chunks
-    static constexpr int kStagesV = 2;                 // 128-column V groups
-    static constexpr int kKBytes = 128 * 64 * 2;       // 16 KB
-    static constexpr int kVBytes = 128 * 128 * 2;      // 32 KB (two 64-column boxes)
+    static constexpr int kStagesK = LatentRings<NP>::k;  // K slots
+    static constexpr int kStagesV = LatentRings<NP>::v;  // 128-column V groups
+    static constexpr int kKChunks = kLatentKChunksPerCopy;  // 64-column chunks per K slot
+    static constexpr int kKCopies = kQChunks / kKChunks;    // K copies per block
+    static constexpr int kKBytes = kKChunks * 128 * 64 * 2;  // 48 KB
+    static constexpr int kVBytes = 128 * 128 * 2;            // 32 KB (two 64-column chunks)
     static constexpr int kQChunkBytes = NP * 128;      // NP rows x 64 columns
     static constexpr int kPBuf = NP * 128 * 2;
+    static constexpr int kPBufs = LatentRings<NP>::p;
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kStagesK * kKBytes;
     static constexpr int kOffQ = kOffV + kStagesV * kVBytes;
     static constexpr int kOffP = kOffQ + kQChunks * kQChunkBytes;
-    static constexpr int kOffRed = kOffP + 2 * kPBuf;      // float red[4][NP]
+    static constexpr int kOffRed = kOffP + kPBufs * kPBuf;  // float red[4][NP]
     static constexpr int kOffM = kOffRed + 4 * NP * 4;     // float m[NP]
     static constexpr int kOffAlpha = kOffM + NP * 4;       // float alpha[NP]
     static constexpr int kOffL = kOffAlpha + NP * 4;       // float l[NP]
@@ -73,7 +91,7 @@ struct LatentCfg {
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;
-    static constexpr int kTmemCols = (6 * NP <= 128) ? 128 : 256;  // S^T x 2, O_g^T x 4
+    static constexpr int kTmemCols = (6 * NP <= 128) ? 128 : (6 * NP <= 256) ? 256 : 512;  // S^T x 2, O_g^T x 4
     static_assert(kSmemAlloc <= 232448, "shared memory budget");
     static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kQChunkBytes % 1024 == 0 && kPBuf % 1024 == 0,
                   "UMMA operands need 1024-byte alignment");
@@ -81,7 +99,8 @@ struct LatentCfg {
 
 template <int NP, class Seqs>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_latent_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmKV,
+    fwd_latent_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ Seqs seqs) {
     using C = LatentCfg<NP>;
     constexpr int KST = C::kStagesK;
@@ -150,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_pfull(i), 128);
             mbar_init(bar_odone(i), 1);
         }
-        mbar_init(bar_qfull, 128);
+        mbar_init(bar_qfull, 1);
         mbar_init(bar_never, 1);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -160,7 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) tma_prefetch_desc(&tmKV);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+    }
+    if (warp == 6 && lane == 0) tma_prefetch_desc(&tmV);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -173,42 +196,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
     const int y0 = kv_off + br.lo * 128;  // first latent row of the range
 
-    if (warp == 0) {
-        // ===================== producer: per block j the 9 K chunks of block j,
-        // then the 4 V groups of block j - 1 (the order the MMA warp consumes them)
+    if (warp == 0 || warp == 6) {
+        // ===================== producers: warp 0 streams the 9 K chunks of
+        // every block, warp 6 the 4 V groups, each through its own ring, so a
+        // K chunk never waits behind a V slot (and the reverse).
         const bool leader = elect_one();
         const uint64_t pol = l2_policy_evict_last();  // rows are read twice (as K, then as V)
         const int where = (kKernDecode << 8) | kSiteProducerEmpty;
-        // Ring positions count the copies issued; a wait that gives up ends the loop.
-        int kpos = 0, vpos = 0;
-        bool ok = true;
-        auto load_k = [&](int j, int c) {
-            const int s = kpos % KST, u = kpos / KST;
-            ok = __all_sync(0xffffffffu, u < 1 || mbar_wait(bar_kempty(s), (u - 1) & 1, wc, where));
-            if (!ok) return;
-            if (leader) {
-                mbar_arrive_expect_tx(bar_kfull(s), C::kKBytes);
-                tma_load_2d(stage_k(s), &tmKV, bar_kfull(s), c * 64, y0 + j * 128, pol);
-            }
-            ++kpos;
-        };
-        auto load_v = [&](int j, int g) {
-            const int s = vpos % VST, u = vpos / VST;
-            ok = __all_sync(0xffffffffu, u < 1 || mbar_wait(bar_vempty(s), (u - 1) & 1, wc, where));
-            if (!ok) return;
-            if (leader) {
-                mbar_arrive_expect_tx(bar_vfull(s), C::kVBytes);
-                tma_load_2d(stage_v(s), &tmKV, bar_vfull(s), g * 128, y0 + j * 128, pol);
-                tma_load_2d(stage_v(s) + 16384, &tmKV, bar_vfull(s), g * 128 + 64, y0 + j * 128, pol);
-            }
-            ++vpos;
-        };
-        for (int j = 0; j <= nblocks && ok; ++j) {
-            for (int c = 0; c < kQChunks && ok && j < nblocks; ++c) load_k(j, c);
-            for (int g = 0; g < kVGroups && ok && j >= 1; ++g) load_v(j - 1, g);
+        const bool is_k = warp == 0;
+        const int slots = is_k ? KST : VST;
+        const uint32_t full0 = is_k ? bar_kfull(0) : bar_vfull(0);
+        const uint32_t empty0 = is_k ? bar_kempty(0) : bar_vempty(0);
+        const uint32_t base = is_k ? stage_k(0) : stage_v(0);
+        const uint32_t stride = is_k ? uint32_t(C::kKBytes) : uint32_t(C::kVBytes);
+        const int per_block = is_k ? C::kKCopies : kVGroups;
+        const CUtensorMap* tm = is_k ? &tmK : &tmV;
+        // Q^T first (warp 0): the tile's packed rows are consecutive rows of the
+        // [B * q_len * Hq][576] query tensor; rows past the tile's last valid
+        // row are padding (their scores are discarded), rows past the tensor
+        // arrive as zeros.
+        const bool q_issued = is_k && nblocks > 0;
+        if (q_issued && leader) {
+            constexpr uint32_t kQBytes = uint32_t(kQChunks * C::kQChunkBytes);
+            const int qrow = (b * p.sq) * p.Hq + m0;
+            mbar_arrive_expect_tx(bar_qfull, kQBytes);
+#pragma unroll
+            for (int c3 = 0; c3 < 3; ++c3)
+                tma_load_3d(sQ + uint32_t(3 * c3 * C::kQChunkBytes), &tmQ, bar_qfull, 0, qrow, 3 * c3,
+                            l2_policy_evict_first());
         }
-        drain_ring(KvRing{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST}, kpos, wc.limit_ns);
-        drain_ring(KvRing{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST}, vpos, wc.limit_ns);
+        // Ring positions count the copies issued; a wait that gives up ends the loop.
+        int pos = 0;
+        for (int j = 0; j < nblocks; ++j) {
+            bool ok = true;
+            for (int c = 0; c < per_block; ++c) {
+                const int sl = pos % slots, u = pos / slots;
+                ok = __all_sync(0xffffffffu, u < 1 || mbar_wait(empty0 + 8u * sl, (u - 1) & 1, wc, where));
+                if (!ok) break;
+                if (leader) {
+                    const uint32_t dst = base + uint32_t(sl) * stride, bar = full0 + 8u * sl;
+                    const int y = y0 + j * 128;
+                    // K copy c: chunks kKChunks c .. kKChunks (c + 1) - 1; V copy c:
+                    // chunks 2c, 2c + 1 (value columns 128c .. 128c + 127).
+                    mbar_arrive_expect_tx(bar, stride);
+                    tma_load_3d(dst, tm, bar, 0, y, is_k ? c * C::kKChunks : 2 * c, pol);
+                }
+                ++pos;
+            }
+            if (!ok) break;
+        }
+        drain_ring(KvRing{base, stride, full0, empty0, slots}, pos, wc.limit_ns);
+        if (q_issued) mbar_drain(bar_qfull, 0, wc.limit_ns);
     } else if (warp == 1) {
         // ===================== MMA issuer (whole warp; one elected lane issues)
         const bool leader = elect_one();
@@ -227,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kpos = 0, vpos = 0;
         for (int j = 0; j <= nblocks; ++j) {
             if (j < nblocks) {
-                for (int c = 0; c < kQChunks; ++c, ++kpos) {
+                for (int c3 = 0; c3 < C::kKCopies; ++c3, ++kpos) {
                     const int s = kpos % KST;
                     const bool good =
                         mbar_wait(bar_kfull(s), (kpos / KST) & 1, wc, (kKernDecode << 8) | kSiteMmaFull);
@@ -236,10 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) {
                         if (good && ok) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t a = kdesc0 + uint64_t((s * C::kKBytes + kk * 32) >> 4);
-                                const uint64_t bd = qdesc0 + uint64_t((c * C::kQChunkBytes + kk * 32) >> 4);
-                                umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, (c > 0 || kk > 0) ? 1u : 0u);
+                            for (int cc = 0; cc < C::kKChunks; ++cc) {
+                                const int c = c3 * C::kKChunks + cc;
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t a =
+                                        kdesc0 + uint64_t((s * C::kKBytes + cc * 16384 + kk * 32) >> 4);
+                                    const uint64_t bd = qdesc0 + uint64_t((c * C::kQChunkBytes + kk * 32) >> 4);
+                                    umma_bf16(tS0 + (j & 1) * NP, a, bd, idesc_qk, (c > 0 || kk > 0) ? 1u : 0u);
+                                }
                             }
                         }
                         umma_commit(bar_kempty(s));
@@ -267,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint64_t a = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
                                 const uint64_t bd =
-                                    pdesc0 + uint64_t(((jj & 1) * C::kPBuf + kk * 2 * (NP / 8) * 128) >> 4);
+                                    pdesc0 + uint64_t(((jj % C::kPBufs) * C::kPBuf + kk * 2 * (NP / 8) * 128) >> 4);
                                 umma_bf16(tO + g * NP, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
@@ -281,53 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (leader) umma_commit(bar_drain);
         mbar_drain(bar_drain, 0, p.timeout_ns);
-    } else {
+    } else if (warp <= 5) {
         // ===================== softmax / correction / epilogue (128 threads)
         const int sidx = threadIdx.x - 64;
         const int kt = 32 * (warp & 3) + lane;  // TMEM lane: key kt of S^T, value column kt of O_g^T
         const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
         const int diag_shift = sk - p.sq;
 
-        // Q tile -> smem: 9 K-major 128B-swizzled chunks of NP rows x 64 columns;
-        // padded rows are zero.
-        {
-            constexpr int kGran = kDq / 8;  // 72 granules of 16 bytes per row
-            constexpr int kTotal = NP * kGran;
-            constexpr int kBatch = 9;
-            for (int base = 0; base < kTotal; base += 128 * kBatch) {
-                uint4 val[kBatch];
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int idx = base + sidx + u * 128;
-                    const int r = idx / kGran;
-                    const int gr = idx - r * kGran;
-                    val[u] = make_uint4(0, 0, 0, 0);
-                    if (idx < kTotal && r < rows_valid) {
-                        const RowMap rm = map_row(p, 0, m0 + r);
-                        val[u] = __ldg(reinterpret_cast<const uint4*>(
-                            p.q + ((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * kDq + gr * 8));
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int idx = base + sidx + u * 128;
-                    if (idx < kTotal) {
-                        const int r = idx / kGran;
-                        const int gr = idx - r * kGran;
-                        const uint32_t dst = sQ + (gr >> 3) * C::kQChunkBytes + sw128_offset(r, gr & 7);
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(val[u].x),
-                                     "r"(val[u].y), "r"(val[u].z), "r"(val[u].w)
-                                     : "memory");
-                    }
-                }
-            }
-        }
         if (sidx < NP) {
             sm_m[sidx] = -INFINITY;
             sm_diag[sidx] = (sidx < rows_valid) ? map_row(p, 0, m0 + sidx).i + diag_shift : 0;
         }
-        fence_proxy_async_smem();
-        mbar_arrive(bar_qfull);
         named_bar_sync(1, 128);
 
         const int diag_lo = (rows_valid > 0) ? sm_diag[0] : 0;
@@ -438,12 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_t[2 * e + 1] += p1;
                 pk[e] = pack_bf16x2(p0, p1);
             }
-            if (j >= 2) {
-                mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+            // P buffer j % kPBufs was last read by the PV of block j - kPBufs.
+            if (j >= C::kPBufs) {
+                const int jp = j - C::kPBufs;
+                mbar_wait(bar_odone(jp & 1), (jp >> 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
             {
-                const uint32_t dst = p_st + uint32_t((j & 1) * C::kPBuf);
+                const uint32_t dst = p_st + uint32_t((j % C::kPBufs) * C::kPBuf);
 #pragma unroll
                 for (int g = 0; g < NP / 8; ++g)
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + g * 128), "r"(pk[4 * g]),
@@ -527,36 +536,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int NP, class Seqs>
-cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmKV, const Seqs& seqs,
-                       cudaStream_t stream) {
+cudaError_t launch_one(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const CUtensorMap& tmQ, const Seqs& seqs, cudaStream_t stream) {
     using C = LatentCfg<NP>;
     auto kern = fwd_latent_kernel<NP, Seqs>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(plan.grid_x, plan.grid_y, plan.grid_z);
-    return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmKV,
-                      seqs);
+    return launch_pdl(reinterpret_cast<const void*>(kern), grid, dim3(kThreads), C::kSmemAlloc, stream, p, tmK,
+                      tmV, tmQ, seqs);
 }
 
 template <class Seqs>
-cudaError_t dispatch(const Plan& plan, const FwdParams& p, const CUtensorMap& tmKV, const Seqs& seqs,
-                     cudaStream_t stream) {
-    if (plan.kBlockM == 16) return launch_one<16>(plan, p, tmKV, seqs, stream);
-    if (plan.kBlockM == 32) return launch_one<32>(plan, p, tmKV, seqs, stream);
+cudaError_t dispatch(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                     const CUtensorMap& tmQ, const Seqs& seqs, cudaStream_t stream) {
+    if (plan.kBlockM == 16) return launch_one<16>(plan, p, tmK, tmV, tmQ, seqs, stream);
+    if (plan.kBlockM == 32) return launch_one<32>(plan, p, tmK, tmV, tmQ, seqs, stream);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_latent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmKV, cudaStream_t stream) {
+cudaError_t launch_latent(const Plan& plan, const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap& tmQ, cudaStream_t stream) {
     if (!plan.latent || plan.d != kDq || plan.dv != kDv || plan.kBlockN != 128) return cudaErrorInvalidValue;
     if (!plan.varlen) {
         UniformSeqs u{plan.kv_len[0], plan.splits_b[0]};
-        return dispatch(plan, p, tmKV, u, stream);
+        return dispatch(plan, p, tmK, tmV, tmQ, u, stream);
     }
     VarlenSeqs v;
     fill_varlen(plan, &v);
-    return dispatch(plan, p, tmKV, v, stream);
+    return dispatch(plan, p, tmK, tmV, tmQ, v, stream);
 }
 
 }  // namespace sk

@@ -201,7 +201,9 @@ sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host
     p.path = path;
     p.kBlockN = 128;
     if (path == SK_PATH_LATENT) {
-        p.kBlockM = p.rows <= 16 ? 16 : 32;  // packed rows per tile; keys on the MMA M axis
+        // Packed rows per tile (keys on the MMA M axis): 32 is the most that
+        // leaves room for the K and V rings next to Q^T.
+        p.kBlockM = p.rows <= 16 ? 16 : 32;
     } else if (path == SK_PATH_DECODE) {
         p.kBlockM = std::max(16, (p.rows + 15) / 16 * 16);
     } else {

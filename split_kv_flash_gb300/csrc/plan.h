@@ -67,6 +67,7 @@ sk_status make_plan_latent(int B, int Hq, int q_len, const int* kv_len_host, int
                            std::string* why);
 constexpr int kLatentDqk = 576;  // 512 latent + 64 rotary columns
 constexpr int kLatentDv = 512;
+constexpr int kLatentKChunksPerCopy = 3;  // 64-column K chunks per TMA copy (9 per 128-key block)
 
 // Host-side range table (see sk_attn_plan_ranges).
 void plan_ranges(const Plan& p, int32_t* out);

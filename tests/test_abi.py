@@ -186,6 +186,7 @@ def test_latent_plan(sk):
         assert info.o_part_offset - info.lse_part_offset >= rows * 4
         assert info.workspace_bytes - info.o_part_offset >= rows * 512 * 4
     assert sk.sk_attn_plan_latent(1, 8, 2, [4096], opts=o).kBlockM == 16
+    assert sk.sk_attn_plan_latent(1, 16, 2, [4096], opts=o).kBlockM == 32
     # one query head: nothing to pack, one head tile of q_len rows
     one = sk.sk_attn_plan_latent(1, 1, 5, [300], opts=o)
     assert one.pack_gqa == 0 and one.rows_per_head_tile == 5 and one.path == sk.SK_PATH_LATENT

@@ -491,6 +491,6 @@ const char* sk_attn_status_string(sk_status s) {
 
 const char* sk_attn_last_error(void) { return g_last_error.c_str(); }
 
-int sk_attn_version(void) { return 101; }
+int sk_attn_version(void) { return 102; }
 
 }  // extern "C"

@@ -53,14 +53,15 @@ template <int HD, int NP>
 struct DecodeCfg {
     // Ring depths: the next QK^T waits on a K block, so K gets the deeper ring;
     // V has a softmax pass of slack.  Each (HD, NP) takes what shared memory allows.
-    static constexpr int kStagesK = HD == 128 ? 3 : 4;
-    static constexpr int kStagesV = HD == 128 ? (NP <= 32 ? 3 : 2) : (NP <= 32 ? 4 : 3);
+    static constexpr int kStagesK = decode_stages_k(HD, NP);
+    static constexpr int kStagesV = decode_stages_v(HD, NP);
     static constexpr int kKBytes = 128 * HD * 2;      // K block: 128 rows x HD
     static constexpr int kVBytes = 128 * 128 * 2;     // V block region: 128 rows x 128 (M = 128 for PV)
     static constexpr int kVLoadBytes = 128 * HD * 2;  // bytes actually loaded
     static constexpr int kQBytes = NP * HD * 2;
     static constexpr int kPBuf = NP * 128 * 2;             // one P^T buffer
-    static constexpr int kPBytes = 2 * kPBuf;                // double-buffered
+    static constexpr int kPBufs = decode_p_bufs(HD, NP);
+    static constexpr int kPBytes = kPBufs * kPBuf;
     static constexpr int kOffK = 0;                        // K ring: kStagesK slots
     static constexpr int kOffV = kStagesK * kKBytes;       // V ring: kStagesV slots
     static constexpr int kOffQ = kOffV + kStagesV * kVBytes;
@@ -341,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t a = vdesc0 + uint64_t((s * C::kVBytes + kk * 2048) >> 4);
-                    const uint64_t bd = pdesc0 + uint64_t(((jj & 1) * C::kPBuf + kk * 2 * (NP / 8) * 128) >> 4);
+                    const uint64_t bd =
+                        pdesc0 + uint64_t(((jj % C::kPBufs) * C::kPBuf + kk * 2 * (NP / 8) * 128) >> 4);
                     umma_bf16(tO, a, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(bar_odone(jj & 1));
@@ -542,15 +544,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_t[2 * e + 1] += p1;
                 pk[e] = pack_bf16x2(p0, p1);
             }
-            // P buffer (j & 1) was last read by the PV of block j - 2.
-            if (j >= 2) {
-                mbar_wait(bar_odone(j & 1), ((j >> 1) - 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
+            // P buffer j % kPBufs was last read by the PV of block j - kPBufs.
+            if (j >= C::kPBufs) {
+                const int jp = j - C::kPBufs;
+                mbar_wait(bar_odone(jp & 1), (jp >> 1) & 1, wc, (kKernDecode << 8) | kSiteSoftmaxODone);
                 tc_fence_after();
             }
             // P^T -> smem, MN-major without swizzle: key kt's 8 consecutive rows
             // form one 16-byte line of a core matrix ([key / 8][row / 8][key % 8][row % 8]).
             {
-                const uint32_t dst = p_st + uint32_t((j & 1) * C::kPBuf);
+                const uint32_t dst = p_st + uint32_t((j % C::kPBufs) * C::kPBuf);
 #pragma unroll
                 for (int g = 0; g < NP / 8; ++g)
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + g * 128), "r"(pk[4 * g]),

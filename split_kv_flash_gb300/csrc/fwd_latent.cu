@@ -10,9 +10,10 @@
 // sit on the tcgen05 M axis ("swap AB"):
 //   S^T[128 x NP]  = sum over 9 column chunks c of K_c[128 x 64] . Q_c^T[64 x NP]
 //   O_g^T[128 x NP] += V_g^T[128 x 128] . P^T[128 x NP],  g = 0..3 (128 value columns each)
-// K arrives in 64-column chunks through a 6-slot ring; V arrives in 128-column
-// groups through a 2-slot ring, loaded from the same latent rows (the second
-// read of a row hits L2).  Online softmax, masks, split epilogue and bounded
+// K arrives as copies of three 64-column chunks (48 KB) through a 2-slot ring;
+// V arrives as one 32 KB copy per 128-column group through a 2- or 3-slot ring,
+// loaded from the same latent rows (the second read of a row hits L2).  Q^T
+// arrives by TMA as well.  Online softmax, masks, split epilogue and bounded
 // waits are those of the decode kernel (fwd_decode.cu).
 //
 // Warp roles (224 threads): warp 0 TMA producer of K chunks, warp 6 of V

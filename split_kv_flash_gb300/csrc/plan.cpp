@@ -257,7 +257,11 @@ sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host
     // measured faster (it merges a tile's rows on many SMs at once).
     if (p.needs_combine && p.path == SK_PATH_DECODE && opts.combine_mode == SK_COMBINE_IN_KERNEL) {
         const long long staged = (long long)p.num_splits * p.rows * d * 4;
-        p.fused_combine = staged <= decode_ring_bytes(d, p.kBlockM);
+        // The merge stages the partials in the K/V rings and its weights
+        // (rows x splits floats) in the P^T buffers.
+        const long long weights = (long long)p.num_splits * p.rows * 4;
+        p.fused_combine = staged <= decode_ring_bytes(d, p.kBlockM) &&
+                          weights <= (long long)decode_p_bufs(d, p.kBlockM) * p.kBlockM * 128 * 2;
     }
 
     // Persistent prefill (tiling chapter sections 4.3-4.4): one CTA per SM over

@@ -18,10 +18,11 @@ constexpr int kMaxSplits = 128;         // the combine kernel merges at most 128
 
 // Shared-memory rings of the decode kernel (K and V slots of 128 rows), also
 // needed by the scheduler: the in-kernel merge stages a tile's partials there.
-constexpr int decode_stages_k(int hd) { return hd == 128 ? 3 : 4; }
+constexpr int decode_stages_k(int hd, int np) { return hd == 128 ? 3 : 4; }
 constexpr int decode_stages_v(int hd, int np) { return hd == 128 ? (np <= 32 ? 3 : 2) : (np <= 32 ? 4 : 3); }
+constexpr int decode_p_bufs(int hd, int np) { return 2; }  // P^T buffers of NP x 128 bf16
 constexpr int decode_ring_bytes(int hd, int np) {
-    return decode_stages_k(hd) * 128 * hd * 2 + decode_stages_v(hd, np) * 128 * 128 * 2;
+    return decode_stages_k(hd, np) * 128 * hd * 2 + decode_stages_v(hd, np) * 128 * 128 * 2;
 }
 
 struct Plan {

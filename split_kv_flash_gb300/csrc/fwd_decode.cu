@@ -575,7 +575,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) red[(warp & 3) * NP + q] = v;
         }
         named_bar_sync(1, 128);
-        if (sidx < NP) sm_l[sidx] = red[sidx] + red[NP + sidx] + red[2 * NP + sidx] + red[3 * NP + sidx];
+        // One thread per row: the row's LSE, 1 / l (into sm_l) and the element
+        // offset of its output row (into red, free once the sums are read).  The
+        // stores below then carry no per-row index arithmetic: with every row
+        // unrolled that arithmetic made the epilogue long enough that, run once
+        // per CTA from a cold instruction cache, it took longer than the loop.
+        const bool final_out = (sb == 1);
+        long long* row_off = reinterpret_cast<long long*>(red);
+        float l_row = 0.f;
+        if (sidx < NP) l_row = red[sidx] + red[NP + sidx] + red[2 * NP + sidx] + red[3 * NP + sidx];
+        named_bar_sync(1, 128);
+        if (sidx < NP) {
+            const int q = sidx;
+            long long off = 0;
+            if (q < rows_valid) {
+                const RowMap rm = map_row(p, ht, m0 + q);
+                const float lse = l_row > 0.f ? (sm_m[q] + log2f(l_row)) * kLn2 : -INFINITY;
+                if (final_out) {
+                    off = ((long long)(size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD;
+                    p.lse[(size_t(b) * p.Hq + rm.h) * p.sq + rm.i] = lse;
+                } else {
+                    const size_t prow = ((size_t(tc.split) * p.B + b) * p.Hq + rm.h) * p.sq + rm.i;
+                    off = (long long)prow * HD;
+                    p.lse_part[prow] = lse;
+                }
+            }
+            row_off[q] = off;
+            sm_l[q] = l_row > 0.f ? 1.f / l_row : 0.f;
+        }
         named_bar_sync(1, 128);
 
         float o[NP];
@@ -589,24 +616,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < NP / 16; ++c) tmem_ld16(tO + lane_off + c * 16, o + c * 16);
             tmem_wait_ld();
         }
-        const bool final_out = (sb == 1);
+        if (kt < HD) {
+            if (final_out) {
 #pragma unroll
-        for (int q = 0; q < NP; ++q) {
-            if (q < rows_valid) {
-                const RowMap rm = map_row(p, ht, m0 + q);
-                const float l = sm_l[q];
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const float val = l > 0.f ? o[q] * inv : 0.f;
-                const float lse = l > 0.f ? (sm_m[q] + log2f(l)) * kLn2 : -INFINITY;
-                if (final_out) {
-                    if (kt < HD)
-                        p.out[((size_t(b) * p.sq + rm.i) * p.Hq + rm.h) * HD + kt] = __float2bfloat16_rn(val);
-                    if (kt == 0) p.lse[(size_t(b) * p.Hq + rm.h) * p.sq + rm.i] = lse;
-                } else {
-                    const size_t prow = ((size_t(tc.split) * p.B + b) * p.Hq + rm.h) * p.sq + rm.i;
-                    if (kt < HD) p.o_part[prow * HD + kt] = val;
-                    if (kt == 0) p.lse_part[prow] = lse;
-                }
+                for (int q = 0; q < NP; ++q)
+                    if (q < rows_valid) p.out[row_off[q] + kt] = __float2bfloat16_rn(o[q] * sm_l[q]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    if (q < rows_valid) p.o_part[row_off[q] + kt] = o[q] * sm_l[q];
             }
         }
         if (!final_out && p.fused_combine)

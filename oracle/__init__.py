@@ -51,6 +51,14 @@ def lib():
                                         ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                         ctypes.c_int, ctypes.c_int, f64p, f64p, ctypes.c_int]
         L.oracle_attn_fwd_v.restype = ctypes.c_int
+        f32p = ctypes.POINTER(ctypes.c_float)
+        L.oracle_gla_fwd.argtypes = [u16p, u16p, u16p, f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_double, f64p, f64p, ctypes.c_int]
+        L.oracle_gla_fwd.restype = ctypes.c_int
+        L.oracle_gla_fwd_segments.argtypes = [u16p, u16p, u16p, f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, f64p,
+                                              ctypes.c_int]
+        L.oracle_gla_fwd_segments.restype = ctypes.c_int
         L.oracle_count_visible.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.oracle_count_visible.restype = ctypes.c_longlong
         _lib = L
@@ -181,3 +189,48 @@ def attn_rows_v(q, k, v, kv_len, scale, rows, causal=False, window_left=-1, nthr
 
 def count_visible(sq, sk, causal, window_left=-1):
     return int(lib().oracle_count_visible(int(sq), int(sk), int(causal), int(window_left)))
+
+
+# ------------------------------------------------------------ linear attention
+# Gated linear attention with a decay per key channel (linear_attn_oracle.c):
+#   S_t = Diag(exp(g_t)) S_{t-1} + k_t v_t^T,  o_t = scale * S_t^T q_t,  S_0 = 0.
+
+def _f32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def gla_fwd(q, k, v, g, scale, nthreads=0):
+    """Token-by-token recurrence.  q, k [B, T, H, dk] and v [B, T, H, dv] as bf16
+    bits (uint16); g [B, T, H, dk] float32.  Returns (out [B, T, H, dv],
+    final state [B, H, dk, dv]) as float64."""
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    g, gp = _f32(g)
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    state = np.zeros((B, H, dk, dv), dtype=np.float64)
+    rc = lib().oracle_gla_fwd(qp, kp, vp, gp, B, T, H, dk, dv, float(scale), _f64p(out), _f64p(state),
+                              int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gla_fwd rejected its arguments")
+    return out, state
+
+
+def gla_fwd_segments(q, k, v, g, scale, nseg, nthreads=0):
+    """The segment method (per-segment (M, h_ext), affine combine, re-run from
+    each segment's incoming state).  Returns out [B, T, H, dv] float64."""
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    g, gp = _f32(g)
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    rc = lib().oracle_gla_fwd_segments(qp, kp, vp, gp, B, T, H, dk, dv, float(scale), int(nseg), _f64p(out),
+                                       int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_gla_fwd_segments rejected its arguments")
+    return out

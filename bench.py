@@ -74,6 +74,8 @@ def named_workloads():
     ws["prefill_local1024"] = wl.prefill(True)
     for w in latent_workloads():
         ws[w.name.replace("latent_verify_", "latent_")] = w
+    for w in linear_workloads():
+        ws[w.name] = w
     return ws
 
 
@@ -82,6 +84,18 @@ def run_named(sk, name, calls, device):
     drawn on the device; checks the device status word at the end."""
     w = named_workloads()[name]
     g = torch.Generator(device=device).manual_seed(w.seed)
+    if isinstance(w, wl.LinearWorkload):
+        shape = (w.B, w.T, w.H, w.d)
+        q = torch.randn(shape, device=device, generator=g).to(torch.bfloat16)
+        k = torch.nn.functional.normalize(torch.randn(shape, device=device, generator=g), dim=-1).to(torch.bfloat16)
+        v = torch.randn(shape, device=device, generator=g).to(torch.bfloat16)
+        gd = -w.gmax * torch.rand(shape, device=device, generator=g)
+        out, ws = sk.linear_attn_fwd(q, k, v, gd, w.scale)
+        for _ in range(calls):
+            sk.linear_attn_fwd(q, k, v, gd, w.scale, out=out, workspace=ws)
+        torch.cuda.synchronize(device)
+        print(json.dumps({"workload": w.name, "calls": calls + 1, "status": "ok"}), flush=True)
+        return
     if isinstance(w, wl.LatentWorkload):
         q = torch.randn((w.B, w.q_len, w.Hq, w.d), device=device, generator=g).to(torch.bfloat16)
         kv = (torch.randn((w.total_kv, w.d), device=device, generator=g) * w.kv_scale).to(torch.bfloat16)
@@ -594,6 +608,64 @@ def latent_summary(rows):
     return flat
 
 
+def linear_workloads():
+    """Chunk-parallel gated linear attention: the cuLA issue's worst case (B=1,
+    H=4, T=8192), a longer sequence and two larger grids."""
+    return [wl.linear_attn(1, 8192, 4), wl.linear_attn(1, 16384, 4), wl.linear_attn(2, 4096, 8),
+            wl.linear_attn(8, 4096, 16)]
+
+
+def linear_flops(w):
+    """Per token and head: the state update (3 flops per state element: a S + k v)
+    and the output (2 per element), dk = dv = 128."""
+    return 5.0 * w.d * w.d * w.B * w.T * w.H
+
+
+ALU_FP32_TFLOPS_PER_SM_GHZ = 128 * 2 / 1e3  # FP32 FMA lanes per SM x 2 flops, TFLOP/s per GHz
+
+
+def gpu_linear(sk, device, clock_mhz, reps=10):
+    """Lone calls (L2 flushed before each) at the planned segment count and, for
+    the speedup the issue reports, with one segment per (sequence, head)."""
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    alu_peak = ALU_FP32_TFLOPS_PER_SM_GHZ * sms * clock_mhz / 1e3
+    rows = []
+    for w in linear_workloads():
+        g_ = torch.Generator(device=device).manual_seed(w.seed)
+        shape = (w.B, w.T, w.H, w.d)
+        q = torch.randn(shape, device=device, generator=g_).to(torch.bfloat16)
+        k = torch.nn.functional.normalize(torch.randn(shape, device=device, generator=g_), dim=-1).to(torch.bfloat16)
+        v = torch.randn(shape, device=device, generator=g_).to(torch.bfloat16)
+        g = -w.gmax * torch.rand(shape, device=device, generator=g_)
+        row = {"workload": w.name}
+        for tag, n in (("", 0), ("one_segment_", 1)):
+            info = sk.sk_linear_attn_plan(w.B, w.T, w.H, num_segments=n)
+            out, ws = sk.linear_attn_fwd(q, k, v, g, w.scale, n)
+            ms = []
+            for i in range(reps):
+                flush.fill_(float(i))
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                sk.linear_attn_fwd(q, k, v, g, w.scale, n, out=out, workspace=ws, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                ms.append(e0.elapsed_time(e1))
+            m = statistics.median(ms)
+            row[tag + "us"] = m * 1e3
+            row[tag + "segments"] = info.num_segments
+            if not tag:
+                row["tokens_per_s"] = w.B * w.T * w.H / (m * 1e-3)
+                row["tflops"] = linear_flops(w) / (m * 1e-3) / 1e12
+                row["frac_of_alu_peak"] = row["tflops"] / alu_peak
+        row["speedup_vs_one_segment"] = row["one_segment_us"] / row["us"]
+        rows.append(row)
+        del q, k, v, g, out, ws
+    return rows, alu_peak
+
+
 def sweep_summary(rows):
     """Flat scalars (per workload: isolated and loop microseconds and fractions
     of the HBM peak), plus the worst row of each kind."""
@@ -841,6 +913,14 @@ def main():
                       "bytes = latent rows once + Q + O + LSE",
             **latent_summary(lrows)}
         result["latent_rows"] = lrows
+        lin, alu_peak = gpu_linear(sk, device, clocks.get("sm_mhz") or 2070.0)
+        result["linear"] = {
+            "unit": "us per call (L2 flushed), tokens x heads per s, TFLOP/s and fraction of the FP32 FMA peak",
+            "bound": "alu", "peak_tflops": alu_peak,
+            "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x the SM clock sampled during the run",
+            "flop_count": "5 dk dv per token and head (state update 3, output 2)",
+            **{r["workload"].replace("gla_", "") + "_" + k: (round(v, 4) if isinstance(v, float) else v)
+               for r in lin for k, v in r.items() if k != "workload"}}
         result["host_us_per_call"] = host_cost_us(sk, device)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_oracle(w, args.cpu_seconds)

@@ -201,6 +201,38 @@ sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* ls
                              void* workspace, size_t ws_bytes, void* cuda_stream,
                              const sk_attn_opts* opts);
 
+/* Chunk-parallel linear attention (inclusionAI/cuLA issue #11: each (sequence,
+ * head) is split along T into N segments that run in parallel and are merged
+ * by an affine combine (M, h_ext)).  The issue does not print the recurrence;
+ * this library computes gated linear attention with one decay per key channel,
+ * for every sequence b and head h:
+ *     S_0 = 0,  S_t = Diag(exp(g_t)) S_{t-1} + k_t v_t^T  (dk x dv, fp32)
+ *     o_t = scale * S_t^T q_t
+ * A segment started from S_in ends at M S_in + h_ext with M = Diag(exp(sum of g
+ * over the segment)) and h_ext its end state from a zero start; segment s covers
+ * tokens [s L, min((s + 1) L, T)), L = ceil(T / N).
+ *   - q, k [B, T, H, dk] bf16;  v [B, T, H, dv] bf16;  g [B, T, H, dk] fp32 log
+ *     decays (<= 0);  out [B, T, H, dv] bf16.  dk = dv = 128 only.
+ *   - num_segments: 0 = one wave of SMs over the (segment, head, sequence) CTAs
+ *     with at least 64 tokens per segment; > 0 = that many (at most T).
+ *   - workspace: >= info.workspace_bytes, 256-byte aligned, caller-owned (the
+ *     segments' h_ext / incoming states and log M); q, k, v, g, out 16-byte
+ *     aligned.  Same error rules as sk_attn_fwd; no device waits, so no timeout
+ *     status.  The state is never returned. */
+typedef struct {
+    int num_segments;        /* N actually used */
+    int segment_len;         /* L */
+    size_t workspace_bytes;
+    int launches;            /* 1 (N = 1) or 3 (segment pass, combine, output pass) */
+} sk_linear_attn_info;
+
+sk_status sk_linear_attn_plan(int B, int T, int H, int dk, int dv, int num_segments,
+                              const sk_attn_opts* opts, sk_linear_attn_info* info);
+sk_status sk_linear_attn_fwd(const void* q, const void* k, const void* v, const float* g, void* out,
+                             int B, int T, int H, int dk, int dv, float scale, int num_segments,
+                             void* workspace, size_t ws_bytes, void* cuda_stream,
+                             const sk_attn_opts* opts);
+
 /* Copy n_int32 int32 of the plan echo (written when opts.debug_echo_plan = 1;
  * same layout as sk_attn_plan_ranges) to host memory.  Synchronises cuda_stream. */
 sk_status sk_attn_read_plan_echo(const void* workspace, int32_t* ranges_host, size_t n_int32,

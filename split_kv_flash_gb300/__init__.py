@@ -17,7 +17,8 @@ __all__ = [
     "sk_attn_fwd_noalloc", "sk_attn_noalloc_status", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
     "SK_PATH_PREFILL", "SK_PATH_LATENT", "sk_attn_plan_latent", "sk_attn_fwd_latent", "attn_fwd_latent",
-    "LATENT_DQK", "LATENT_DV", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
+    "LATENT_DQK", "LATENT_DV", "LinearAttnInfo", "sk_linear_attn_plan", "sk_linear_attn_fwd",
+    "linear_attn_fwd", "LINEAR_ATTN_DIM", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
     "SK_SCHEDULE_ONE_TILE", "SK_SCHEDULE_PERSISTENT", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
 ]
@@ -67,6 +68,14 @@ class PlanInfo(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class LinearAttnInfo(ctypes.Structure):
+    _fields_ = [("num_segments", ctypes.c_int), ("segment_len", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t), ("launches", ctypes.c_int)]
+
+
+LINEAR_ATTN_DIM = 128  # dk = dv of the linear-attention entry points
+
+
 class SKError(RuntimeError):
     def __init__(self, status, where=""):
         self.status = status
@@ -100,12 +109,17 @@ def lib():
                                           ctypes.POINTER(PlanInfo)]
         L.sk_attn_fwd_latent.argtypes = [vp, vp, vp, vp, ci, ci, ci, _intp, ci, ci, cf, ci, ci, vp, sz,
                                          vp, ctypes.POINTER(Opts)]
+        L.sk_linear_attn_plan.argtypes = [ci, ci, ci, ci, ci, ci, ctypes.POINTER(Opts),
+                                          ctypes.POINTER(LinearAttnInfo)]
+        L.sk_linear_attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, sz, vp,
+                                         ctypes.POINTER(Opts)]
         L.sk_attn_read_plan_echo.argtypes = [vp, _i32p, sz, vp]
         L.sk_attn_workspace_status.argtypes = [vp, vp, _intp]
         L.sk_attn_noalloc_status.argtypes = [vp, _intp]
         for f in ("sk_attn_plan", "sk_attn_plan_ranges", "sk_attn_fwd", "sk_attn_fwd_noalloc",
                   "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_noalloc_status",
-                  "sk_attn_plan_latent", "sk_attn_fwd_latent"):
+                  "sk_attn_plan_latent", "sk_attn_fwd_latent", "sk_linear_attn_plan",
+                  "sk_linear_attn_fwd"):
             getattr(L, f).restype = ci
         L.sk_attn_status_string.argtypes = [ci]
         L.sk_attn_status_string.restype = ctypes.c_char_p
@@ -323,3 +337,51 @@ def attn_fwd_latent(q, kv, kv_len, scale=None, causal=False, window_left=-1, out
     sk_attn_fwd_latent(q, kv, out, lse, B, Hq, sq, kv_len, LATENT_DQK, LATENT_DV, scale, causal, window_left,
                        workspace, workspace.numel(), stream, opts)
     return out, lse, workspace
+
+
+def sk_linear_attn_plan(B, T, H, dk=LINEAR_ATTN_DIM, dv=LINEAR_ATTN_DIM, num_segments=0, opts=None):
+    info = LinearAttnInfo()
+    _check(lib().sk_linear_attn_plan(B, T, H, dk, dv, num_segments,
+                                     ctypes.byref(opts) if opts is not None else None, ctypes.byref(info)))
+    return info
+
+
+def sk_linear_attn_fwd(q, k, v, g, out, B, T, H, dk, dv, scale, num_segments, workspace, ws_bytes, stream=None,
+                       opts=None):
+    """Pointer-level chunk-parallel gated linear attention call."""
+    if stream is not None and not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _check(lib().sk_linear_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), B, T, H, dk, dv, float(scale),
+                                    int(num_segments), _ptr(workspace), int(ws_bytes), stream,
+                                    ctypes.byref(opts) if opts is not None else None))
+
+
+def linear_attn_fwd(q, k, v, g, scale=None, num_segments=0, out=None, workspace=None, opts=None, stream=None):
+    """Convenience wrapper over sk_linear_attn_fwd for torch CUDA tensors.
+
+    q, k [B, T, H, 128], v [B, T, H, 128] bf16; g [B, T, H, 128] fp32 log decays.
+    Returns (out [B, T, H, 128] bf16, workspace)."""
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k and v must be bfloat16")
+    if g.dtype != torch.float32:
+        raise TypeError("g must be float32")
+    for t in (q, k, v, g):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v and g must be contiguous CUDA tensors")
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    if tuple(k.shape) != (B, T, H, dk) or tuple(g.shape) != (B, T, H, dk) or tuple(v.shape[:3]) != (B, T, H):
+        raise ValueError("shape mismatch between q, k, v and g")
+    if scale is None:
+        scale = 1.0 / float(dk) ** 0.5
+    info = sk_linear_attn_plan(B, T, H, dk, dv, num_segments, opts)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(int(info.workspace_bytes), 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sk_linear_attn_fwd(q, k, v, g, out, B, T, H, dk, dv, scale, num_segments, workspace, workspace.numel(),
+                       stream, opts)
+    return out, workspace

@@ -12,6 +12,7 @@
 
 #include "../../include/sk_attn.h"
 #include "fwd_common.cuh"
+#include "linear_attn.h"
 #include "plan.h"
 
 namespace sk {
@@ -448,6 +449,72 @@ sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* ls
     g_last_error.clear();
     return fwd_impl(q, kv, kv, out, lse, B, Hq, 1, q_len, kv_len_host, d_qk, d_v, true, scale, causal,
                     window_left, workspace, ws_bytes, cuda_stream, opts);
+}
+
+namespace {
+sk_status linear_plan(int B, int T, int H, int dk, int dv, int num_segments, const sk_attn_opts* opts,
+                      sk::LinearAttnPlan* lp) {
+    if (dk != kLinearAttnDim || dv != kLinearAttnDim)
+        return fail(SK_ERR_UNSUPPORTED, "linear attention: dk = dv = 128 only");
+    if (B <= 0 || H <= 0 || T < 0 || num_segments < 0) return fail(SK_ERR_INVALID_ARG, "bad B, H, T or segments");
+    if ((long long)B * T * H >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "B * T * H must be < 2^31");
+    int sms = opts && opts->num_sms > 0 ? opts->num_sms : 0;
+    if (sms == 0) {
+        DeviceInfo di;
+        sk_status s = current_device(&di);
+        if (s != SK_OK) return s;
+        sms = di.sms;
+    }
+    make_linear_attn_plan(B, T, H, num_segments, sms, lp);
+    return SK_OK;
+}
+}  // namespace
+
+sk_status sk_linear_attn_plan(int B, int T, int H, int dk, int dv, int num_segments, const sk_attn_opts* opts,
+                              sk_linear_attn_info* info) {
+    g_last_error.clear();
+    if (!info) return fail(SK_ERR_INVALID_ARG, "info is NULL");
+    sk::LinearAttnPlan lp;
+    sk_status s = linear_plan(B, T, H, dk, dv, num_segments, opts, &lp);
+    if (s != SK_OK) return s;
+    memset(info, 0, sizeof *info);
+    info->num_segments = lp.N;
+    info->segment_len = lp.L;
+    info->workspace_bytes = lp.ws_bytes;
+    info->launches = lp.N > 1 ? 3 : 1;
+    return SK_OK;
+}
+
+sk_status sk_linear_attn_fwd(const void* q, const void* k, const void* v, const float* g, void* out, int B, int T,
+                             int H, int dk, int dv, float scale, int num_segments, void* workspace, size_t ws_bytes,
+                             void* cuda_stream, const sk_attn_opts* opts) {
+    g_last_error.clear();
+    if (!isfinite(scale)) return fail(SK_ERR_INVALID_ARG, "scale must be finite");
+    DeviceInfo di;
+    sk_status s = current_device(&di);
+    if (s != SK_OK) return s;
+    if (!(di.major == 10 && di.minor == 3))
+        return fail(SK_ERR_UNSUPPORTED, "this library runs on sm_103 (GB300) only");
+    sk::LinearAttnPlan lp;
+    s = linear_plan(B, T, H, dk, dv, num_segments, opts, &lp);
+    if (s != SK_OK) return s;
+    if (T == 0) return SK_OK;
+    if (!q || !k || !v || !g || !out || !workspace) return fail(SK_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) || !aligned(out, 16))
+        return fail(SK_ERR_MISALIGNED, "q, k, v, g and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(SK_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    if (ws_bytes < lp.ws_bytes) return fail(SK_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than info.workspace_bytes");
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    cudaError_t e;
+    if (opts && opts->event_begin &&
+        (e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_begin), stream)) != cudaSuccess)
+        return fail_cuda(e, "cudaEventRecord");
+    e = launch_linear_attn(lp, q, k, v, g, out, workspace, scale, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "linear attention launch");
+    if (opts && opts->event_end &&
+        (e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), stream)) != cudaSuccess)
+        return fail_cuda(e, "cudaEventRecord");
+    return SK_OK;
 }
 
 sk_status sk_attn_read_plan_echo(const void* workspace, int32_t* ranges_host, size_t n_int32, void* cuda_stream) {

@@ -1,0 +1,84 @@
+"""GPU parity of the chunk-parallel gated linear attention (cuLA issue #11:
+T split into segments merged by an affine combine) through the C ABI against
+the fp64 oracle's token-by-token recurrence.
+
+Tolerance, per element: |o - o_ref| <= 2^-8 |o_ref| + 1e-3.  The output is
+bf16 (half a unit in the last place is at most 2^-9 |o|); the fp32 state adds
+a relative error of about 1e-6 over the few hundred tokens a decay of at most
+e^-0.1 per token keeps in memory, well inside the absolute term."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sk():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    return H.sk_mod()
+
+
+def _check(sk, w, num_segments=0, calls=1):
+    q, k, v, g = wl.make_linear_inputs(w)
+    ref, _ = oracle.gla_fwd(wl.bits(q), wl.bits(k), wl.bits(v), g.numpy(), w.scale)
+    qg, kg, vg, gg = q.cuda(), k.cuda(), v.cuda(), g.cuda()
+    out, ws = sk.linear_attn_fwd(qg, kg, vg, gg, w.scale, num_segments)
+    for call in range(calls):
+        if call:
+            out.zero_()
+            sk.linear_attn_fwd(qg, kg, vg, gg, w.scale, num_segments, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        o = out.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(o))
+        err = np.abs(o - ref) - (2.0 ** -8 * np.abs(ref) + 1e-3)
+        assert float(err.max()) <= 0.0, "%s N=%d call %d: max|dO| %.3e (max|O| %.3e)" % (
+            w.name, num_segments, call, float(np.abs(o - ref).max()), float(np.abs(ref).max()))
+    return sk.sk_linear_attn_plan(w.B, w.T, w.H, num_segments=num_segments)
+
+
+def test_page_worst_case_shape_auto_segments(sk):
+    """B=1, H=4, T=8192 (the issue's worst case): one wave of segments."""
+    info = _check(sk, wl.linear_attn(1, 8192, 4), 0, calls=2)
+    assert info.num_segments > 1 and info.launches == 3
+
+
+@pytest.mark.parametrize("nseg", [1, 2, 5, 16, 37])
+def test_segment_counts(sk, nseg):
+    """Any segment count gives the recurrence's result (1 = no split)."""
+    info = _check(sk, wl.linear_attn(2, 1111, 3, seed=1710), nseg)
+    L = -(-1111 // nseg)
+    assert info.segment_len == L and info.num_segments == -(-1111 // L)  # empty trailing segments dropped
+
+
+@pytest.mark.parametrize("B,T,H,nseg", [
+    (1, 1, 1, 0),        # one token
+    (1, 33, 2, 0),       # one chunk and one token
+    (1, 40, 1, 40),      # one token per segment
+    (3, 517, 5, 0),      # ragged chunks, several sequences and heads
+    (1, 300, 2, 7),      # segments that end inside a staged chunk
+])
+def test_edges(sk, B, T, H, nseg):
+    _check(sk, wl.LinearWorkload("gla_edge_b%d_t%d_h%d" % (B, T, H), B, T, H, seed=1720 + T), nseg)
+
+
+def test_errors(sk):
+    w = wl.linear_attn(1, 64, 1)
+    q, k, v, g = [t.cuda() for t in wl.make_linear_inputs(w)]
+    out = torch.empty_like(v)
+    info = sk.sk_linear_attn_plan(1, 64, 1, num_segments=2)
+    ws = torch.empty(int(info.workspace_bytes), dtype=torch.uint8, device="cuda")
+    with pytest.raises(sk.SKError) as ei:  # workspace too small
+        sk.sk_linear_attn_fwd(q, k, v, g, out, 1, 64, 1, 128, 128, w.scale, 2, ws, 16)
+    assert ei.value.status == 3
+    with pytest.raises(sk.SKError) as ei:  # head dim outside the supported set
+        sk.sk_linear_attn_plan(1, 64, 1, 64, 64)
+    assert ei.value.status == 2
+    with pytest.raises(sk.SKError) as ei:  # misaligned output
+        sk.sk_linear_attn_fwd(q, k, v, g, out.data_ptr() + 2, 1, 64, 1, 128, 128, w.scale, 2, ws, ws.numel())
+    assert ei.value.status == 4

@@ -157,3 +157,37 @@ def latent_verify(B: int, Hq: int, q_len: int, kv_len, causal: bool = True, seed
     return LatentWorkload("latent_verify_b%d_h%d_q%d_kv%s%s" % (B, Hq, q_len, "-".join(map(str, sorted(set(kv)))),
                                                              "" if causal else "_nomask"),
                           B, Hq, q_len, kv, causal=causal, seed=seed)
+
+
+@dataclass
+class LinearWorkload:
+    """Chunk-parallel gated linear attention (cuLA issue #11 shapes)."""
+    name: str
+    B: int
+    T: int
+    H: int
+    seed: int = 0
+    d: int = 128
+    gmax: float = 0.1
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.d))
+
+
+def make_linear_inputs(w: LinearWorkload):
+    """(q, k, v, g) on the CPU: q, v standard normal, k standard normal scaled to
+    unit L2 norm per token and head, all rounded to bf16; g float32 log decays
+    drawn uniform in [-gmax, 0]."""
+    gen = torch.Generator().manual_seed(w.seed)
+    shape = (w.B, w.T, w.H, w.d)
+    q = torch.randn(shape, generator=gen, dtype=torch.float32)
+    k = torch.randn(shape, generator=gen, dtype=torch.float32)
+    v = torch.randn(shape, generator=gen, dtype=torch.float32)
+    g = -w.gmax * torch.rand(shape, generator=gen, dtype=torch.float32)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), g
+
+
+def linear_attn(B: int, T: int, H: int, seed: int = 1700) -> LinearWorkload:
+    return LinearWorkload("gla_b%d_t%d_h%d_d128" % (B, T, H), B, T, H, seed=seed)

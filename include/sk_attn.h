@@ -2,7 +2,8 @@
  * sk_attn.h -- C ABI of the split-KV flash attention forward library for
  * GB300 (sm_103a).  Library: split_kv_flash_gb300/libskattn.so.
  *
- * Operation (what every entry point below computes or plans):
+ * Operation (what every entry point below computes or plans; the latent and
+ * linear-attention entry points near the end state their own):
  *   tiled attention forward with online softmax, parallelised over the KV axis
  *   (flash-decoding).  For batch b, query head h and query row i:
  *     O[b,i,h,:] = sum_j softmax_j(scale * <Q[b,i,h,:], K[off_b+j, h/G, :]>) V[off_b+j, h/G, :]

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_segment_kernel(const __grid_c
 
 // In place over hs: slot s goes from h_s to S_in(s).  One thread per state
 // element, 256 elements per CTA; the segment loads do not depend on the chain
-// and are issued ahead of it (unrolled).
+// and are issued 16 segments at a time, ahead of it.
 __global__ void __launch_bounds__(256) gla_combine_kernel(const __grid_constant__ LaParams p) {
     const int e = blockIdx.x * 256 + threadIdx.x;   // element of the 128 x 128 state
     const int h = blockIdx.y, b = blockIdx.z;
@@ -252,25 +252,23 @@ __global__ void __launch_bounds__(256) gla_combine_kernel(const __grid_constant_
     const float* lm = p.logm + (size_t(b) * p.H + h) * kD + row;
     const size_t lstride = size_t(p.B) * p.H * kD;
     float acc = 0.f;   // S_in(s)
-    int s = 0;
-    for (; s + 4 <= p.N; s += 4) {
-        float hv[4], m[4];
+    constexpr int kU = 16;  // segments whose loads are in flight together
+    for (int s0 = 0; s0 < p.N; s0 += kU) {
+        float hv[kU], m[kU];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            hv[u] = s + u < p.N - 1 ? hp[(s + u) * stride] : 0.f;
-            m[u] = s + u < p.N - 1 ? __expf(lm[(s + u) * lstride]) : 0.f;
+        for (int u = 0; u < kU; ++u) {
+            const int s = s0 + u;
+            hv[u] = s < p.N - 1 ? hp[s * stride] : 0.f;
+            m[u] = s < p.N - 1 ? lm[s * lstride] : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            hp[(s + u) * stride] = acc;
-            acc = fmaf(m[u], acc, hv[u]);
+        for (int u = 0; u < kU; ++u) {
+            const int s = s0 + u;
+            if (s < p.N) {
+                hp[s * stride] = acc;
+                acc = fmaf(__expf(m[u]), acc, hv[u]);
+            }
         }
-    }
-    for (; s < p.N; ++s) {
-        const float hv = s < p.N - 1 ? hp[s * stride] : 0.f;
-        const float m = s < p.N - 1 ? __expf(lm[s * lstride]) : 0.f;
-        hp[s * stride] = acc;
-        acc = fmaf(m, acc, hv);
     }
 }
 

@@ -21,9 +21,10 @@
 // 7 16-byte shared loads
 // (k, the decays and q of its rows, v of its columns) and the output's sum
 // over rows is a reduction over the 16 lanes of a half-warp.  Tokens
-// are staged in shared memory 32 at a time (k, v, q converted to fp32, the
-// decays exponentiated once per token and channel), double-buffered through
-// registers.
+// are staged in shared memory 32 at a time (k, v, q converted to fp32), the
+// next chunk's loads in flight in registers meanwhile; within a chunk the state
+// is carried rescaled by the chunk's cumulative decay (see Stage), so a token
+// costs one FMA per state element.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -55,11 +56,21 @@ struct LaParams {
 };
 
 // Shared-memory staging of one chunk: fp32 k, exp(g), v and (output pass) q.
+// With cum_t = sum of g over the chunk's tokens up to t (per key channel), the
+// state is carried as S'_t = S_t / exp(cum_t) inside a chunk, so a token costs
+// one FMA per state element: S'_t = S'_{t-1} + (k_t exp(-cum_t)) v_t^T, and
+// o_t = scale * S'_t^T (q_t exp(cum_t)); at the chunk's end S = S' exp(cum_end).
+// A chunk in which some cum_t leaves [kCumFloor, -kCumFloor] (exp(-cum_t) would
+// approach the ends of the fp32 range) runs the plain update S = exp(g) S + k v^T.
+constexpr float kCumFloor = -60.f;
+
 struct Stage {
-    float k[kTC][kD];
-    float a[kTC][kD];
+    float k[kTC][kD];    // k, then (rescaled chunks) k exp(-cum)
+    float q[kTC][kD];    // q, then (rescaled chunks) q exp(cum)
     float v[kTC][kD];
-    float q[kTC][kD];
+    float g[kTC][kD];    // raw log decays
+    float a[kTC][kD];    // exp(g) (plain chunks)
+    float ecend[kD];     // exp(cum at the chunk's last token)
 };
 
 // Register copy of one chunk's raw inputs for thread tid (loaded ahead of use).
@@ -125,44 +136,84 @@ __device__ __forceinline__ void store_stage(const Raw& r, Stage& s, bool with_q,
         const int e = tid + kThreads * u;
         const int tg = e / 32, c4 = (e % 32) * 4;
         const float gv[4] = {r.g[u].x, r.g[u].y, r.g[u].z, r.g[u].w};
+        *reinterpret_cast<float4*>(&s.g[tg][c4]) = r.g[u];
         *reinterpret_cast<float4*>(&s.a[tg][c4]) = make_float4(__expf(gv[0]), __expf(gv[1]), __expf(gv[2]), __expf(gv[3]));
 #pragma unroll
         for (int i = 0; i < 4; ++i) gsum[i] += gv[i];
     }
 }
 
+// After the chunk is staged: channel c = tid (tid < 128) accumulates cum over
+// the chunk's n tokens; unless some channel's cum leaves [kCumFloor, -kCumFloor]
+// (then the chunk takes the plain update, which this returns to every thread),
+// each channel rescales its k (and q) column.
+template <bool OUT>
+__device__ __forceinline__ bool rescale_chunk(Stage& s, int n) {
+    const int c = threadIdx.x;
+    bool out_of_range = false;
+    if (c < kD) {
+        float cum = 0.f;
+        for (int t = 0; t < n; ++t) {
+            cum += s.g[t][c];
+            out_of_range |= cum < kCumFloor || cum > -kCumFloor;
+        }
+    }
+    const bool plain = __syncthreads_or(out_of_range) != 0;
+    if (!plain) {
+        if (c < kD) {
+            float cum = 0.f;
+            for (int t = 0; t < n; ++t) {
+                cum += s.g[t][c];
+                s.k[t][c] *= __expf(-cum);
+                if (OUT) s.q[t][c] *= __expf(cum);
+            }
+            s.ecend[c] = __expf(cum);
+        }
+        __syncthreads();
+    }
+    return plain;
+}
+
 // One pass over tokens [t0, t1) of (b, h) on the state S held in registers;
 // with OUT the outputs o_t go to global memory (staged per chunk).
 template <bool OUT>
 __device__ __forceinline__ void run_tokens(const LaParams& p, int b, int h, int t0, int t1, float (&S)[kS],
-                                           Stage* st, float* gsum, __nv_bfloat16 (*osm)[kD]) {
+                                           Stage& s, float* gsum, __nv_bfloat16 (*osm)[kD]) {
     const int tid = threadIdx.x;
     const int rg = tid & 15, cg = tid >> 4;
     const int nch = (t1 - t0 + kTC - 1) / kTC;
     Raw raw;
     if (nch > 0) load_raw(p, b, h, t0, t1, OUT, raw);
     for (int c = 0; c < nch; ++c) {
-        Stage& s = st[c & 1];
         store_stage(raw, s, OUT, gsum);
         __syncthreads();
         const int c0 = t0 + c * kTC;
         const int n = min(kTC, t1 - c0);
         if (c + 1 < nch) load_raw(p, b, h, c0 + kTC, t1, OUT, raw);  // next chunk, in flight during this one
+        const bool plain = rescale_chunk<OUT>(s, n);
         // Two tokens per iteration: the next token's state update overlaps this
         // token's output reduction.
 #pragma unroll 2
         for (int t = 0; t < n; ++t) {
             const float4 v4 = *reinterpret_cast<const float4*>(&s.v[t][kC * cg]);
             const float vv[kC] = {v4.x, v4.y, v4.z, v4.w};
-            float kk[kR], aa[kR];
+            float kk[kR];
             *reinterpret_cast<float4*>(&kk[0]) = *reinterpret_cast<const float4*>(&s.k[t][4 * rg]);
             *reinterpret_cast<float4*>(&kk[4]) = *reinterpret_cast<const float4*>(&s.k[t][64 + 4 * rg]);
-            *reinterpret_cast<float4*>(&aa[0]) = *reinterpret_cast<const float4*>(&s.a[t][4 * rg]);
-            *reinterpret_cast<float4*>(&aa[4]) = *reinterpret_cast<const float4*>(&s.a[t][64 + 4 * rg]);
+            if (plain) {
+                float aa[kR];
+                *reinterpret_cast<float4*>(&aa[0]) = *reinterpret_cast<const float4*>(&s.a[t][4 * rg]);
+                *reinterpret_cast<float4*>(&aa[4]) = *reinterpret_cast<const float4*>(&s.a[t][64 + 4 * rg]);
 #pragma unroll
-            for (int i = 0; i < kR; ++i)
+                for (int i = 0; i < kR; ++i)
 #pragma unroll
-                for (int jj = 0; jj < kC; ++jj) S[i * kC + jj] = fmaf(aa[i], S[i * kC + jj], kk[i] * vv[jj]);
+                    for (int jj = 0; jj < kC; ++jj) S[i * kC + jj] = fmaf(aa[i], S[i * kC + jj], kk[i] * vv[jj]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kR; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < kC; ++jj) S[i * kC + jj] = fmaf(kk[i], vv[jj], S[i * kC + jj]);
+            }
             if (OUT) {
                 float qq[kR];
                 *reinterpret_cast<float4*>(&qq[0]) = *reinterpret_cast<const float4*>(&s.q[t][4 * rg]);
@@ -182,6 +233,15 @@ __device__ __forceinline__ void run_tokens(const LaParams& p, int b, int h, int 
                     *reinterpret_cast<__nv_bfloat162*>(&osm[t][kC * cg]) = lo;
                     *reinterpret_cast<__nv_bfloat162*>(&osm[t][kC * cg + 2]) = hi;
                 }
+            }
+        }
+        if (!plain) {
+            // back from S' to S: rows scaled by exp(cum at the chunk's end)
+#pragma unroll
+            for (int i = 0; i < kR; ++i) {
+                const float e = s.ecend[state_row(rg, i)];
+#pragma unroll
+                for (int jj = 0; jj < kC; ++jj) S[i * kC + jj] *= e;
             }
         }
         __syncthreads();
@@ -217,8 +277,8 @@ __device__ __forceinline__ void load_state(const float* src, float (&S)[kS]) {
 
 __global__ void __launch_bounds__(kThreads, 1) gla_segment_kernel(const __grid_constant__ LaParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    Stage* st = reinterpret_cast<Stage*>(smem_raw);
-    float* gred = reinterpret_cast<float*>(smem_raw + 2 * sizeof(Stage));  // [16][128]
+    Stage& st = *reinterpret_cast<Stage*>(smem_raw);
+    float* gred = reinterpret_cast<float*>(smem_raw + sizeof(Stage));  // [16][128]
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int t0 = s * p.L, t1 = min(p.T, (s + 1) * p.L);
     float S[kS];
@@ -274,8 +334,8 @@ __global__ void __launch_bounds__(256) gla_combine_kernel(const __grid_constant_
 
 __global__ void __launch_bounds__(kThreads, 1) gla_output_kernel(const __grid_constant__ LaParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    Stage* st = reinterpret_cast<Stage*>(smem_raw);
-    auto osm = reinterpret_cast<__nv_bfloat16(*)[kD]>(smem_raw + 2 * sizeof(Stage));
+    Stage& st = *reinterpret_cast<Stage*>(smem_raw);
+    auto osm = reinterpret_cast<__nv_bfloat16(*)[kD]>(smem_raw + sizeof(Stage));
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int t0 = s * p.L, t1 = min(p.T, (s + 1) * p.L);
     float S[kS];
@@ -288,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) gla_output_kernel(const __grid_co
 
 }  // namespace
 
-size_t linear_attn_smem_segment() { return 2 * sizeof(Stage) + 16 * kD * sizeof(float); }
-size_t linear_attn_smem_output() { return 2 * sizeof(Stage) + kTC * kD * sizeof(__nv_bfloat16); }
+size_t linear_attn_smem_segment() { return sizeof(Stage) + 16 * kD * sizeof(float); }
+size_t linear_attn_smem_output() { return sizeof(Stage) + kTC * kD * sizeof(__nv_bfloat16); }
 
 cudaError_t launch_linear_attn(const LinearAttnPlan& lp, const void* q, const void* k, const void* v,
                                const float* g, void* out, void* workspace, float scale, cudaStream_t stream) {

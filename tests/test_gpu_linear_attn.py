@@ -82,3 +82,13 @@ def test_errors(sk):
     with pytest.raises(sk.SKError) as ei:  # misaligned output
         sk.sk_linear_attn_fwd(q, k, v, g, out.data_ptr() + 2, 1, 64, 1, 128, 128, w.scale, 2, ws, ws.numel())
     assert ei.value.status == 4
+
+
+@pytest.mark.parametrize("gmax", [0.01, 1.5, 8.0])
+def test_decay_strengths(sk, gmax):
+    """Weak decays (rescaled chunks only), decays whose chunk sums cross the
+    rescaling range in some chunks (mixed), and strong decays (every chunk on the
+    plain update)."""
+    w = wl.LinearWorkload("gla_gmax%g" % gmax, 2, 700, 3, seed=1730, gmax=gmax)
+    _check(sk, w, 0)
+    _check(sk, w, 5)

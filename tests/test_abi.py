@@ -175,12 +175,15 @@ def test_latent_plan(sk):
     16- or 32-row tiles of the one latent head, partials 512 columns wide;
     other widths are refused."""
     o = _opts(sk, num_sms=152)
-    info = sk.sk_attn_plan_latent(2, 64, 9, [521, 521], 576, 512, True, opts=o)
+    info = sk.sk_attn_plan_latent(2, 64, 9, [2065, 2065], 576, 512, True, opts=o)
     assert info.path == sk.SK_PATH_LATENT
     assert info.pack_gqa == 1 and info.head_tiles == 1
     assert info.rows_per_head_tile == 9 * 64 and info.kBlockM == 32
     assert info.num_m_blocks == 18
     assert info.grid_x == 18 and info.grid_y == info.num_splits and info.grid_z == 2
+    # at most 8 KV blocks: 16-row tiles
+    short = sk.sk_attn_plan_latent(2, 64, 9, [521, 521], 576, 512, True, opts=o)
+    assert short.kBlockM == 16 and short.num_m_blocks == 36
     if info.needs_combine:
         rows = info.num_splits * 2 * 64 * 9
         assert info.o_part_offset - info.lse_part_offset >= rows * 4

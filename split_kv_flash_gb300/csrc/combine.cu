@@ -16,7 +16,8 @@
 //  - few splits (S <= 16; verify, batched decode: many rows, few splits): one
 //    warp per row, 8 rows per CTA, lane s holding split s's LSE and lane c the
 //    float4 columns c, c + 32, ... of the row, so a CTA is not launched for a
-//    few loads.
+//    few loads.  The partials of up to 16 splits (8 or 4 for 64- or 512-wide rows) are
+//    loaded at once, next to the LSEs, so the merge costs one L2 round trip.
 // Rows are 64, 128 or 512 values wide (512: latent attention).
 // Both are launched as programmatic dependents of the partial kernel: they are
 // scheduled while the partial kernel runs and wait (griddepcontrol.wait) for
@@ -136,6 +137,8 @@ __global__ void __launch_bounds__(32 * kWarps)
     combine_rows_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ Seqs seqs, long long rows) {
     constexpr int kCols4 = HD / 4;
     constexpr int kPer = (kCols4 + 31) / 32;
+    // splits loaded together: at most 16 float4 a lane (8 for 64-wide rows, whose upper lanes idle)
+    constexpr int kBatch = kPer == 1 ? (HD >= 128 ? kRowsMaxSplits : 8) : 4;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * kWarps + warp;
@@ -151,8 +154,25 @@ __global__ void __launch_bounds__(32 * kWarps)
     const size_t stride = (size_t)p.B * p.Hq * p.sq;  // between splits of one row
     const size_t base = ((size_t)b * p.Hq + h) * p.sq + i;
 
-    // log-sum-exp over the splits: lane s holds split s
+    // lane s holds split s's LSE; lane c the float4 columns c, c + 32, ... of
+    // every split's O partial.  The O loads of kBatch splits are issued together,
+    // the first batch next to the LSE load, so a row with S <= kBatch costs one
+    // L2 round trip.
     const float l = (lane < S) ? __ldcg(p.lse_part + lane * stride + base) : -INFINITY;
+    const float4* src = reinterpret_cast<const float4*>(p.o_part + base * HD) + lane;
+    const size_t stride4 = stride * (HD / 4);
+    float4 v[kBatch][kPer];
+    auto load_batch = [&](int s0) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+            for (int t = 0; t < kPer; ++t)
+                v[u][t] = (s0 + u < S && t * 32 + lane < kCols4) ? __ldcg(src + t * 32 + (s0 + u) * stride4)
+                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load_batch(0);
+
+    // log-sum-exp over the splits
     float mx = l;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -162,25 +182,25 @@ __global__ void __launch_bounds__(32 * kWarps)
     const float lse = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
     const float w = (l == -INFINITY || lse == -INFINITY) ? 0.f : exp2f((l - lse) * kLog2e);
 
-    // weighted sum of the O partials: lane c holds float4 columns c, c + 32, ...
+    // weighted sum of the O partials (lanes >= S carry weight 0)
     float4 acc[kPer];
 #pragma unroll
     for (int t = 0; t < kPer; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + base * HD) + lane;
-    const size_t stride4 = stride * (HD / 4);
-#pragma unroll 4
-    for (int s = 0; s < S; ++s) {
-        const float ws = __shfl_sync(0xffffffffu, w, s);
+    for (int s0 = 0;;) {
 #pragma unroll
-        for (int t = 0; t < kPer; ++t) {
-            if (t * 32 + lane < kCols4) {
-                const float4 v = __ldcg(src + t * 32 + s * stride4);
-                acc[t].x += ws * v.x;
-                acc[t].y += ws * v.y;
-                acc[t].z += ws * v.z;
-                acc[t].w += ws * v.w;
+        for (int u = 0; u < kBatch; ++u) {
+            const float ws = __shfl_sync(0xffffffffu, w, s0 + u);
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                acc[t].x += ws * v[u][t].x;
+                acc[t].y += ws * v[u][t].y;
+                acc[t].z += ws * v[u][t].z;
+                acc[t].w += ws * v[u][t].w;
             }
         }
+        s0 += kBatch;
+        if (s0 >= S) break;
+        load_batch(s0);
     }
 #pragma unroll
     for (int t = 0; t < kPer; ++t) {

@@ -429,22 +429,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_window = p.window_left >= 0;
 
         // Per row q (identical in every thread): neg_m[q] = -(running max) in
-        // log2 units; +inf while the row has no visible key yet (any visible
-        // score then exceeds the threshold and sets the max); -inf for padding
-        // rows, whose scores thereby become -inf and their P 0.  The running max
-        // itself lives in sm_m and is only read on the rare blocks that raise it.
+        // log2 units, 0 while the row has seen no visible key; -1e30 for padding
+        // rows, whose scores thereby fall to -1e30 and their P to 0.  The
+        // running max itself lives in sm_m and is only read on the blocks that
+        // raise it.  Until every valid row has a finite max, every block takes
+        // the rescale path, which sets the max of the rows that start there.
         float l_t[NP];
         float neg_m[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             l_t[q] = 0.f;
-            neg_m[q] = (q < rows_valid) ? INFINITY : -INFINITY;
+            neg_m[q] = (q < rows_valid) ? 0.f : -1e30f;
         }
+        bool unstarted = rows_valid > 0;
         const float sl2 = p.scale_log2;
         const uint32_t p_st = sP + uint32_t((kt >> 3) * (NP / 8) * 128 + (kt & 7) * 16);
-        auto masked = [&](int key, int q) {
-            const int dg = sm_diag[q];
-            return key >= sk || (has_causal && key > dg) || (has_window && key < dg - p.window_left);
+        // The rows that see this thread's key, as bits (bit q: row q), from a
+        // rolled loop over the rows: per-row tests unrolled over the NP rows
+        // made the masked blocks' code so long that a CTA starting on a masked
+        // block spent microseconds fetching it.
+        auto visible_rows = [&](int key) -> unsigned long long {
+            unsigned long long vis = 0ull;
+            if (key < sk) {
+#pragma unroll 4
+                for (int q = 0; q < rows_valid; ++q) {
+                    const int dg = sm_diag[q];
+                    const bool ok = (!has_causal || key <= dg) && (!has_window || key >= dg - p.window_left);
+                    vis |= (unsigned long long)ok << q;
+                }
+            }
+            return vis;
         };
 
         for (int j = 0; j < nblocks; ++j) {
@@ -464,29 +478,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < NP; ++q) t[q] = fmaf(t[q], sl2, neg_m[q]);
             if (need_mask) {
+                const unsigned long long vis = visible_rows(key);
 #pragma unroll
                 for (int q = 0; q < NP; ++q)
-                    if (masked(key, q)) t[q] = -INFINITY;
+                    if (!((vis >> q) & 1ull)) t[q] = -INFINITY;
             }
-            bool need = false;
+            bool need = unstarted;
 #pragma unroll
             for (int q = 0; q < NP; ++q) need |= t[q] > kRescaleThreshold;
             if (named_bar_or(1, 128, need)) {
-                // A row's max grew by more than 2^8 (or its first visible key
-                // arrived): reload the raw scores, take every row's block max,
-                // move the running maxima and recompute the scores.  The S buffer
-                // is only released after this, so the reload reads this block.
-#pragma unroll
-                for (int c = 0; c < NP / 16; ++c) tmem_ld16(tS + c * 16, t + c * 16);
-                tmem_wait_ld();
+                // A row's max grew by more than 2^8, or a row may see its first
+                // key here: take every row's block max (t - neg_m is the scaled
+                // score; -inf where masked), move the running maxima and shift
+                // the scores by the change.
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
-                    float v = t[q] * sl2;
-                    if (need_mask && masked(key, q)) v = -INFINITY;
-                    v = warp_max_f32(v);
+                    const float v = warp_max_f32(t[q] - neg_m[q]);
                     if (lane == 0) red[(warp & 3) * NP + q] = v;
                 }
                 named_bar_sync(1, 128);
+                bool still = false;  // a valid row without a visible key so far
                 if (sidx < NP) {
                     const int q = sidx;
                     float a = 1.f;
@@ -496,23 +507,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float mn = fmaxf(mo, bm);
                         a = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);  // l and O are 0 while mo = -inf
                         sm_m[q] = mn;
+                        still = mn == -INFINITY;
                     }
                     sm_alpha[q] = a;
                 }
-                named_bar_sync(1, 128);
+                unstarted = named_bar_or(1, 128, still);
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     if (q < rows_valid) {
                         const float mq = sm_m[q];
-                        neg_m[q] = (mq == -INFINITY) ? INFINITY : -mq;
+                        const float nm = (mq == -INFINITY) ? 0.f : -mq;
+                        t[q] += nm - neg_m[q];
+                        neg_m[q] = nm;
                     }
                     l_t[q] *= sm_alpha[q];
-                    t[q] = fmaf(t[q], sl2, neg_m[q]);
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int q = 0; q < NP; ++q)
-                        if (masked(key, q)) t[q] = -INFINITY;
                 }
                 // Rescaling O needs the previous block's PV to be complete.
                 if (j >= 1) {

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_latent_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ Seqs seqs) {
+    static_assert(NP <= 32, "the visible-row mask is one 32-bit word");
     using C = LatentCfg<NP>;
     constexpr int KST = C::kStagesK;
     constexpr int VST = C::kStagesV;
@@ -342,18 +343,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int diag_hi = (rows_valid > 0) ? sm_diag[rows_valid - 1] : 0;
         const bool has_causal = p.causal != 0;
         const bool has_window = p.window_left >= 0;
+        // neg_m[q] = -(running max of row q) in log2 units: 0 until the row
+        // sees a key, -1e30 for padding rows (their P is then 0).  Until every
+        // valid row has a finite max, every block takes the rescale path.
         float l_t[NP];
         float neg_m[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             l_t[q] = 0.f;
-            neg_m[q] = (q < rows_valid) ? INFINITY : -INFINITY;
+            neg_m[q] = (q < rows_valid) ? 0.f : -1e30f;
         }
+        bool unstarted = rows_valid > 0;
         const float sl2 = p.scale_log2;
         const uint32_t p_st = sP + uint32_t((kt >> 3) * (NP / 8) * 128 + (kt & 7) * 16);
-        auto masked = [&](int key, int q) {
-            const int dg = sm_diag[q];
-            return key >= sk || (has_causal && key > dg) || (has_window && key < dg - p.window_left);
+        // Rows that see this thread's key, as bits, from a rolled loop (short
+        // code: the masked blocks are often a CTA's first, run from a cold
+        // instruction cache).
+        auto visible_rows = [&](int key) -> unsigned {
+            unsigned vis = 0u;
+            if (key < sk) {
+#pragma unroll 4
+                for (int q = 0; q < rows_valid; ++q) {
+                    const int dg = sm_diag[q];
+                    const bool ok = (!has_causal || key <= dg) && (!has_window || key >= dg - p.window_left);
+                    vis |= unsigned(ok) << q;
+                }
+            }
+            return vis;
         };
 
         for (int j = 0; j < nblocks; ++j) {
@@ -372,25 +388,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < NP; ++q) t[q] = fmaf(t[q], sl2, neg_m[q]);
             if (need_mask) {
+                const unsigned vis = visible_rows(key);
 #pragma unroll
                 for (int q = 0; q < NP; ++q)
-                    if (masked(key, q)) t[q] = -INFINITY;
+                    if (!((vis >> q) & 1u)) t[q] = -INFINITY;
             }
-            bool need = false;
+            bool need = unstarted;
 #pragma unroll
             for (int q = 0; q < NP; ++q) need |= t[q] > kRescaleThreshold;
             if (named_bar_or(1, 128, need)) {
-#pragma unroll
-                for (int c = 0; c < NP / 16; ++c) tmem_ld16(tS + c * 16, t + c * 16);
-                tmem_wait_ld();
+                // Block max of each row from t - neg_m (the scaled score, -inf
+                // where masked), new running maxima, scores shifted by the change.
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
-                    float v = t[q] * sl2;
-                    if (need_mask && masked(key, q)) v = -INFINITY;
-                    v = warp_max_f32(v);
+                    const float v = warp_max_f32(t[q] - neg_m[q]);
                     if (lane == 0) red[(warp & 3) * NP + q] = v;
                 }
                 named_bar_sync(1, 128);
+                bool still = false;
                 if (sidx < NP) {
                     const int q = sidx;
                     float a = 1.f;
@@ -400,23 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float mn = fmaxf(mo, bm);
                         a = (mo == -INFINITY) ? 0.f : fast_exp2(mo - mn);
                         sm_m[q] = mn;
+                        still = mn == -INFINITY;
                     }
                     sm_alpha[q] = a;
                 }
-                named_bar_sync(1, 128);
+                unstarted = named_bar_or(1, 128, still);
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     if (q < rows_valid) {
                         const float mq = sm_m[q];
-                        neg_m[q] = (mq == -INFINITY) ? INFINITY : -mq;
+                        const float nm = (mq == -INFINITY) ? 0.f : -mq;
+                        t[q] += nm - neg_m[q];
+                        neg_m[q] = nm;
                     }
                     l_t[q] *= sm_alpha[q];
-                    t[q] = fmaf(t[q], sl2, neg_m[q]);
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int q = 0; q < NP; ++q)
-                        if (masked(key, q)) t[q] = -INFINITY;
                 }
                 if (j >= 1) {
                     mbar_wait(bar_odone((j - 1) & 1), ((j - 1) >> 1) & 1, wc,

@@ -11,13 +11,14 @@
 // Two shapes of the same merge:
 //  - many splits (S > 16; long-context decode: few rows, up to 128 splits):
 //    one CTA of 8 warps per output row.  The row's partials are spread over
-//    the warps (warp w takes splits w, w + 8, ...), so every load of the row is
-//    in flight at once and the merge costs about one L2 round trip;
+//    the warps (warp w takes splits w, w + 8, ...) and loaded together with
+//    the LSEs, so a 64- or 128-wide row costs about one L2 round trip (a
+//    512-wide row one per 32 splits);
 //  - few splits (S <= 16; verify, batched decode: many rows, few splits): one
 //    warp per row, 8 rows per CTA, lane s holding split s's LSE and lane c the
 //    float4 columns c, c + 32, ... of the row, so a CTA is not launched for a
-//    few loads.  The partials of up to 16 splits (8 or 4 for 64- or 512-wide rows) are
-//    loaded at once, next to the LSEs, so the merge costs one L2 round trip.
+//    few loads.  The partials of up to 16 splits (8 or 4 for 64- or 512-wide
+//    rows) are loaded at once, next to the LSEs: one L2 round trip.
 // Rows are 64, 128 or 512 values wide (512: latent attention).
 // Both are launched as programmatic dependents of the partial kernel: they are
 // scheduled while the partial kernel runs and wait (griddepcontrol.wait) for
@@ -56,6 +57,26 @@ __global__ void __launch_bounds__(32 * kWarps)
     const size_t stride = (size_t)p.B * p.Hq * p.sq;  // between splits of one row
     const size_t base = ((size_t)b * p.Hq + h) * p.sq + i;
 
+    // Warp w takes splits w, w + 8, ...; lane c the float4 columns c, c + 32, ...
+    // A round loads kRound splits a warp (16 float4 a lane); the first round is
+    // issued before the LSE phase so that both loads are in flight together.
+    constexpr int kRound = 16 / kPer;
+    const float4* src0 = reinterpret_cast<const float4*>(p.o_part + base * HD);
+    const size_t stride4 = stride * (HD / 4);
+    float4 v[kRound][kPer];
+    auto load_round = [&](int r) {
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+            const int s = warp + (r * kRound + u) * kWarps;
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                const int c = t * 32 + lane;
+                v[u][t] = (s < S && c < kCols4) ? __ldcg(src0 + c + s * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    load_round(0);
+
     // 1. log-sum-exp over the splits (warp 0), weights into shared memory.
     if (warp == 0) {
         float l[kMaxSplits / 32];
@@ -84,34 +105,28 @@ __global__ void __launch_bounds__(32 * kWarps)
     }
     __syncthreads();
 
-    // 2. weighted sum of the O partials, splits spread over the warps; lane c
-    //    holds float4 columns c, c + 32, ... of the row.
-    const float4* src0 = reinterpret_cast<const float4*>(p.o_part + base * HD);
-    const size_t stride4 = stride * (HD / 4);
-#pragma unroll 1
-    for (int t = 0; t < kPer; ++t) {
-        const int c = t * 32 + lane;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < kCols4) {
-            constexpr int kUnroll = kMaxSplits / kWarps;  // 16
-            float4 v[kUnroll];
+    // 2. weighted sum of this warp's splits, then across the warps.
+    float4 acc[kPer];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int s = warp + u * kWarps;
-                v[u] = (s < S) ? __ldcg(src0 + c + s * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+    for (int t = 0; t < kPer; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int rounds = (S + kWarps * kRound - 1) / (kWarps * kRound);
+    for (int r = 0; r < rounds; ++r) {
+        if (r > 0) load_round(r);
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int s = warp + u * kWarps;
-                const float ws = (s < S) ? w_s[s] : 0.f;
-                acc.x += ws * v[u].x;
-                acc.y += ws * v[u].y;
-                acc.z += ws * v[u].z;
-                acc.w += ws * v[u].w;
+        for (int u = 0; u < kRound; ++u) {
+            const int s = warp + (r * kRound + u) * kWarps;
+            const float ws = (s < S) ? w_s[s] : 0.f;
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) {
+                acc[t].x += ws * v[u][t].x;
+                acc[t].y += ws * v[u][t].y;
+                acc[t].z += ws * v[u][t].z;
+                acc[t].w += ws * v[u][t].w;
             }
         }
-        part[warp][c] = acc;
     }
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) part[warp][t * 32 + lane] = acc[t];
     __syncthreads();
     for (int c = threadIdx.x; c < kCols4; c += 32 * kWarps) {
         float4 t = part[0][c];

@@ -27,6 +27,7 @@ namespace sk {
 namespace {
 
 constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
+constexpr int kDecodeL2Warm = 3;  // K and V blocks of a range prefetched into L2 before the grid dependency
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -277,13 +278,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        // The range's first K and V blocks into L2 while the previous kernel on
+        // the stream may still be running.  Only a hint: global writes land in
+        // L2, so the copies issued after the wait below read current data.
+        // Split calls only: back to back, their partial kernel starts during the
+        // previous call's combine, which leaves the prefetch time to land (GQA
+        // decode, 131072 keys: 49.2 -> 47.0 us a call).  After a single-split
+        // call the grid starts only at that call's epilogue, and the prefetch
+        // measured slower there (verify over 137 keys: 4.9 -> 5.2 us).
+        const int kvh = p.pack_gqa ? ht : ht / p.G;
+        const int npre = sb > 1 ? min(nblocks, kDecodeL2Warm) : 0;
+        for (int j = 0; j < npre; ++j)
+#pragma unroll
+            for (int c = 0; c < HD / 64; ++c) {
+                tma_prefetch_l2_2d(&tmK, kvh * HD + c * 64, kv_off + (br.lo + j) * 128);
+                tma_prefetch_l2_2d(&tmV, kvh * HD + c * 64, kv_off + (br.lo + j) * 128);
+            }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Everything above touched only shared memory, TMEM and kernel parameters.
-    // Under programmatic dependent launch this grid may start while the previous
-    // kernel on the stream is still running: wait for it before any global access.
+    // Everything above read only shared memory, TMEM and kernel parameters (the
+    // L2 prefetch returns nothing).  Under programmatic dependent launch this
+    // grid may start while the previous kernel on the stream is still running:
+    // wait for it before any global access.
     griddep_wait();
     if (p.echo_plan && threadIdx.x == 0)
         *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = make_int4(br.lo, br.hi, int(word), 1);

@@ -246,6 +246,14 @@ sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host
             }
             default:
                 S = fill_policy(p, p.num_sms, max_splits);
+                // Splitting shortens the longest CTA by nblk_max - chunk blocks
+                // and adds the combine kernel; on the decode path that pays
+                // only from kDecodeCombineBlocks blocks on (verify q=9 over 137
+                // keys: one split 4.9 us, two 6.3 us).  Latent blocks take
+                // about 2.5 us each, so that path splits as the fill says.
+                if (S > 1 && p.path == SK_PATH_DECODE &&
+                    p.nblk_max - div_up(p.nblk_max, S) < kDecodeCombineBlocks)
+                    S = 1;
                 break;
         }
         S = std::max(1, std::min(S, max_splits));

@@ -15,6 +15,9 @@ constexpr int kMaxVarlenBatch = 1024;   // per-sequence tables travel as kernel 
 constexpr int kDecodeMaxRows = 64;      // decode path: <= 64 packed rows per tile
 constexpr int kDefaultMaxSplits = 128;
 constexpr int kMaxSplits = 128;         // the combine kernel merges at most 128 partials
+// Decode path: a split must save at least this many 128-key blocks of one CTA's
+// time to pay for the combine kernel (about 2.2 us against 0.75-0.8 us a block).
+constexpr int kDecodeCombineBlocks = 3;
 
 // Shared-memory rings of the decode kernel (K and V slots of 128 rows), also
 // needed by the scheduler: the in-kernel merge stages a tile's partials there.

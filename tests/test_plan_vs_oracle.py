@@ -144,11 +144,25 @@ def test_fill_policy_invariants(sk):
             if info.needs_combine:
                 ctas = sum(c * info.head_tiles * info.num_m_blocks for c in sb)
                 assert ctas <= num_sms
+                if info.path == sk.SK_PATH_DECODE:
+                    # a split pays for the combine only when it saves 3 blocks
+                    nblk = po.ceil_div(max(kv), 128)
+                    assert nblk - po.ceil_div(nblk, S) >= 3
             G = Hq // Hkv
             pack = bool(info.pack_gqa)
             exp = po.cta_table(sq, kv, G, pack, info.head_tiles, info.kBlockM, 128,
                                info.num_m_blocks, info.num_splits, sb, causal, window)
             assert same_table(sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, o), exp)
+
+
+def test_short_verify_keeps_one_split(sk):
+    """Speculative verify (B=2, 16 heads, causal): over 137 or 265 keys the
+    decode path takes one split (the combine would cost more than the blocks
+    it saves); over 2057 keys it splits."""
+    for kv, split in ((137, False), (265, False), (2057, True)):
+        info = sk.sk_attn_plan(2, 16, 16, 9, [kv] * 2, 128, True, -1, _opts(sk, 0, 152))
+        assert info.path == sk.SK_PATH_DECODE
+        assert bool(info.needs_combine) == split, kv
 
 
 def test_gqa_decode_split_counts(sk):

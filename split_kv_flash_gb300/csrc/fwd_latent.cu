@@ -35,6 +35,7 @@ constexpr int kDq = kLatentDqk;        // 576
 constexpr int kDv = kLatentDv;         // 512
 constexpr int kQChunks = kDq / 64;     // 9
 constexpr int kVGroups = kDv / 128;    // 4
+constexpr int kLatentL2Warm = 2;       // latent blocks of a split range prefetched into L2 before the grid dependency
 static_assert(kQChunks % kLatentKChunksPerCopy == 0, "K copies cover whole blocks");
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -184,6 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
+        // A split CTA's first latent blocks into L2 while the previous kernel
+        // on the stream (the previous call's combine) may still be running: a
+        // hint only, global writes land in L2 (as in the decode kernel).  The
+        // values are the same rows, so the K copies cover them.
+        const int npre = sb > 1 ? min(nblocks, kLatentL2Warm) : 0;
+        for (int j = 0; j < npre; ++j)
+#pragma unroll
+            for (int c = 0; c < C::kKCopies; ++c)
+                tma_prefetch_l2_3d(&tmK, 0, kv_off + (br.lo + j) * 128, c * C::kKChunks);
     }
     if (warp == 6 && lane == 0) tma_prefetch_desc(&tmV);
     tc_fence_before();

@@ -399,13 +399,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (c < c_lo || c > c_hi) x[c] = -INFINITY;
             }
+            // Row max: 8 chains of 16 columns, two columns per three-input max.
             float mx8[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) mx8[c] = x[c];
+            for (int k = 0; k < 8; ++k) {
+                float m = fmax3(x[k], x[k + 8], x[k + 16]);
 #pragma unroll
-            for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int c = 24; c < 120; c += 16) m = fmax3(m, x[k + c], x[k + c + 8]);
+                mx8[k] = fmaxf(m, x[k + 120]);
+            }
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                   fmaxf(mx8[6], mx8[7]));
             const float cand = mx * sl2;
             bool rescale = false;
             float alpha = 1.f;
@@ -434,15 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
             // P row -> TMEM (upper half of S_t): 64 columns of packed bf16 pairs.
+            // Scale-and-shift and the row sum run on column pairs (f32x2).
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(fmaf(x[c4 * 32 + 2 * e], sl2, neg_m));
-                    const float p1 = fast_exp2(fmaf(x[c4 * 32 + 2 * e + 1], sl2, neg_m));
-                    ls[(2 * e) & 3] += p0;
-                    ls[(2 * e + 1) & 3] += p1;
+                    float s0, s1;
+                    fma_f32x2(s0, s1, x[c4 * 32 + 2 * e], x[c4 * 32 + 2 * e + 1], sl2, sl2, neg_m, neg_m);
+                    const float p0 = fast_exp2(s0);
+                    const float p1 = fast_exp2(s1);
+                    add_f32x2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                     pk[e] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16u(tS(t) + C::kPCol + lane_off + c4 * 16, pk);

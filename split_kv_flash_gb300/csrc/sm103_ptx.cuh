@@ -352,6 +352,35 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int g) {
     return uint32_t(row) * 128u + (uint32_t(g ^ (row & 7)) << 4);
 }
 
+// Packed FP32 pairs (PTX fma/add .f32x2, sm_100 and later): one instruction
+// for two elements, each rounded as its scalar form would be.
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                          float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 a, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 d, {%0, %1};\n\t"
+        "add.rn.f32x2 d, d, a;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+// Maximum of three floats in one instruction (max.f32 with three sources).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);

@@ -474,8 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (c * 32 + e < c_lo || c * 32 + e > c_hi) x[e] = -INFINITY;
                     }
+                    float ma = mx, mb = -INFINITY;  // two chains, two columns per three-input max
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, x[e]);
+                    for (int e = 0; e < 32; e += 4) {
+                        ma = fmax3(ma, x[e], x[e + 1]);
+                        mb = fmax3(mb, x[e + 2], x[e + 3]);
+                    }
+                    mx = fmaxf(ma, mb);
                 }
                 const float cand = mx * sl2;
                 bool rescale = false;
@@ -518,11 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = fast_exp2(fmaf(x[2 * e], sl2, neg_m));
-                        const float p1 = fast_exp2(fmaf(x[2 * e + 1], sl2, neg_m));
-                        ls[(2 * e) & 3] += p0;
-                        ls[(2 * e + 1) & 3] += p1;
+                    for (int e = 0; e < 16; ++e) {  // scale-and-shift and row sums on f32x2 pairs
+                        float s0, s1;
+                        fma_f32x2(s0, s1, x[2 * e], x[2 * e + 1], sl2, sl2, neg_m, neg_m);
+                        const float p0 = fast_exp2(s0);
+                        const float p1 = fast_exp2(s1);
+                        add_f32x2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                         pk[e] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16u(tS(t) + C::kPCol + lane_off + c4 * 16, pk);

@@ -150,6 +150,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
     auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
+    if (warp == 2 && lane == 0 && nblocks > 0 && p.q_tma) {
+        // While the CTA sets up: the tile's Q into L2, marked evict-first like
+        // its copies below (read once; K/V, re-read by other tiles, keep L2).
+        // Only a hint; global writes land in L2, so the copies after the grid
+        // dependency below still read current data.
+        for (int t = 0; t < kHalves; ++t)
+#pragma unroll
+            for (int c = 0; c < HD / 64; ++c)
+                tma_prefetch_l2_4d_hint(&tmQ, c * 64, 0, ht, b * p.sq + (m0 + 128 * t) / p.q_gp,
+                                        l2_policy_evict_first());
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < KST; ++s) {
             mbar_init(bar_kfull(s), 1);

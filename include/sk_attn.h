@@ -74,7 +74,10 @@ typedef enum {
     SK_PATH_AUTO = 0,
     SK_PATH_DECODE = 1,   /* <= 64 packed query rows per tile: KV rows on the MMA M axis */
     SK_PATH_PREFILL = 2,  /* 256-row tiles: two 128-row halves that share each K/V block; query rows on the MMA M axis */
-    SK_PATH_LATENT = 3    /* latent attention (sk_attn_fwd_latent only): 16 or 32 packed rows per tile, keys on the MMA M axis */
+    SK_PATH_LATENT = 3,   /* latent attention (sk_attn_fwd_latent only): 16 or 32 packed rows per tile, keys on the MMA M axis */
+    SK_PATH_LINEAR_RECURRENT = 4, /* linear attention: the segments run token by token on the FMA pipes */
+    SK_PATH_LINEAR_CHUNK = 5      /* linear attention: the segments run in windows of <= 128 tokens as four
+                                     128 x 128 x 128 tensor-core products each (the default) */
 } sk_path;
 
 /* How the split partials are merged (sk_attn_opts.combine_mode; the stream-k
@@ -215,16 +218,28 @@ sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* ls
  *   - q, k [B, T, H, dk] bf16;  v [B, T, H, dv] bf16;  g [B, T, H, dk] fp32 log
  *     decays (<= 0);  out [B, T, H, dv] bf16.  dk = dv = 128 only.
  *   - num_segments: 0 = one wave of SMs over the (segment, head, sequence) CTAs
- *     with at least 64 tokens per segment; > 0 = that many (at most T).
+ *     with at least 64 tokens per segment (128 on the chunk path); > 0 = that
+ *     many (at most T).
+ *   - opts->force_path: SK_PATH_LINEAR_CHUNK (also for SK_PATH_AUTO) runs each
+ *     segment in windows of at most 128 tokens on the tensor cores: inside a
+ *     window the state, the intra-window scores and the outputs are dense
+ *     products (bf16 operands, fp32 accumulation, the state kept in fp32); a
+ *     window ends before a key channel's summed log decay would span more than
+ *     60, and log decays are clamped to [-100, 100].  SK_PATH_LINEAR_RECURRENT
+ *     runs the recurrence token by token in fp32 on the FMA pipes.  Other values
+ *     are SK_ERR_INVALID_ARG.
  *   - workspace: >= info.workspace_bytes, 256-byte aligned, caller-owned (the
  *     segments' h_ext / incoming states and log M); q, k, v, g, out 16-byte
- *     aligned.  Same error rules as sk_attn_fwd; no device waits, so no timeout
- *     status.  The state is never returned. */
+ *     aligned.  Same error rules as sk_attn_fwd.  The chunk path's device waits
+ *     are bounded by opts->wait_timeout_us; one that gives up leaves its code in
+ *     the workspace's status word (sk_attn_workspace_status), which the call's
+ *     first kernel clears.  The state is never returned. */
 typedef struct {
     int num_segments;        /* N actually used */
     int segment_len;         /* L */
     size_t workspace_bytes;
     int launches;            /* 1 (N = 1) or 3 (segment pass, combine, output pass) */
+    int path;                /* SK_PATH_LINEAR_CHUNK or SK_PATH_LINEAR_RECURRENT */
 } sk_linear_attn_info;
 
 sk_status sk_linear_attn_plan(int B, int T, int H, int dk, int dv, int num_segments,

@@ -16,7 +16,7 @@ __all__ = [
     "sk_attn_read_plan_echo", "sk_attn_workspace_status", "sk_attn_status_string",
     "sk_attn_fwd_noalloc", "sk_attn_noalloc_status", "NOALLOC_SCRATCH_BYTES",
     "sk_attn_last_error", "sk_attn_version", "attn_fwd", "SK_OK", "SK_PATH_DECODE",
-    "SK_PATH_PREFILL", "SK_PATH_LATENT", "sk_attn_plan_latent", "sk_attn_fwd_latent", "attn_fwd_latent",
+    "SK_PATH_PREFILL", "SK_PATH_LATENT", "SK_PATH_LINEAR_RECURRENT", "SK_PATH_LINEAR_CHUNK", "sk_attn_plan_latent", "sk_attn_fwd_latent", "attn_fwd_latent",
     "LATENT_DQK", "LATENT_DV", "LinearAttnInfo", "sk_linear_attn_plan", "sk_linear_attn_fwd",
     "linear_attn_fwd", "LINEAR_ATTN_DIM", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
     "SK_SCHEDULE_ONE_TILE", "SK_SCHEDULE_PERSISTENT", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
@@ -31,6 +31,7 @@ SK_ERR_MISALIGNED, SK_ERR_CUDA, SK_ERR_DEVICE_TIMEOUT = 4, 5, 6
 SK_POLICY_DEFAULT, SK_POLICY_FILL, SK_POLICY_FA_HEURISTIC = 0, 1, 2
 SK_POLICY_FIXED_CHUNK, SK_POLICY_MIN_CHUNK = 3, 4
 SK_PATH_AUTO, SK_PATH_DECODE, SK_PATH_PREFILL, SK_PATH_LATENT = 0, 1, 2, 3
+SK_PATH_LINEAR_RECURRENT, SK_PATH_LINEAR_CHUNK = 4, 5
 LATENT_DQK, LATENT_DV = 576, 512  # latent attention: 512 latent + 64 rotary key columns, 512 value columns
 SK_COMBINE_AUTO, SK_COMBINE_KERNEL, SK_COMBINE_IN_KERNEL = 0, 1, 2
 SK_SCHEDULE_AUTO, SK_SCHEDULE_ONE_TILE, SK_SCHEDULE_PERSISTENT = 0, 1, 2
@@ -70,7 +71,7 @@ class PlanInfo(ctypes.Structure):
 
 class LinearAttnInfo(ctypes.Structure):
     _fields_ = [("num_segments", ctypes.c_int), ("segment_len", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t), ("launches", ctypes.c_int)]
+                ("workspace_bytes", ctypes.c_size_t), ("launches", ctypes.c_int), ("path", ctypes.c_int)]
 
 
 LINEAR_ATTN_DIM = 128  # dk = dv of the linear-attention entry points

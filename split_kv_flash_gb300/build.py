@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["api.cu", "fwd_decode.cu", "fwd_prefill.cu", "fwd_prefill_persistent.cu", "fwd_latent.cu", "combine.cu",
-              "noalloc.cu", "linear_attn.cu"]
+              "noalloc.cu", "linear_attn.cu", "linear_attn_tc.cu"]
 CXX_SOURCES = ["plan.cpp"]
 
 

@@ -112,6 +112,21 @@ bool make_o_map(CUtensorMap* m, void* o, int B, int q_len, int Hq, int d, int gp
     return r == CUDA_SUCCESS;
 }
 
+// Log decays g [rows][H * 128] fp32 as a 2-D tensor; boxes of 128 rows x 128
+// columns (512 bytes) without swizzle, row-major in shared memory.
+bool make_g_map(CUtensorMap* m, const float* base, int H, long long rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cuuint64_t(H) * kLinearAttnDim, cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(H) * kLinearAttnDim * 4};
+    cuuint32_t box[2] = {kLinearAttnDim, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct DeviceInfo {
     int dev = 0, sms = 0, major = 0, minor = 0;
 };
@@ -453,11 +468,15 @@ sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* ls
 
 namespace {
 sk_status linear_plan(int B, int T, int H, int dk, int dv, int num_segments, const sk_attn_opts* opts,
-                      sk::LinearAttnPlan* lp) {
+                      sk::LinearAttnPlan* lp, int* path) {
     if (dk != kLinearAttnDim || dv != kLinearAttnDim)
         return fail(SK_ERR_UNSUPPORTED, "linear attention: dk = dv = 128 only");
     if (B <= 0 || H <= 0 || T < 0 || num_segments < 0) return fail(SK_ERR_INVALID_ARG, "bad B, H, T or segments");
     if ((long long)B * T * H >= (1LL << 31)) return fail(SK_ERR_UNSUPPORTED, "B * T * H must be < 2^31");
+    const int fp = opts ? opts->force_path : SK_PATH_AUTO;
+    if (fp != SK_PATH_AUTO && fp != SK_PATH_LINEAR_CHUNK && fp != SK_PATH_LINEAR_RECURRENT)
+        return fail(SK_ERR_INVALID_ARG, "linear attention: force_path must be AUTO, LINEAR_CHUNK or LINEAR_RECURRENT");
+    *path = fp == SK_PATH_LINEAR_RECURRENT ? int(SK_PATH_LINEAR_RECURRENT) : int(SK_PATH_LINEAR_CHUNK);
     int sms = opts && opts->num_sms > 0 ? opts->num_sms : 0;
     if (sms == 0) {
         DeviceInfo di;
@@ -465,7 +484,8 @@ sk_status linear_plan(int B, int T, int H, int dk, int dv, int num_segments, con
         if (s != SK_OK) return s;
         sms = di.sms;
     }
-    make_linear_attn_plan(B, T, H, num_segments, sms, lp);
+    make_linear_attn_plan(B, T, H, num_segments, sms, lp,
+                          *path == SK_PATH_LINEAR_CHUNK ? kLinearAttnMinSegmentChunk : kLinearAttnMinSegment);
     return SK_OK;
 }
 }  // namespace
@@ -475,13 +495,15 @@ sk_status sk_linear_attn_plan(int B, int T, int H, int dk, int dv, int num_segme
     g_last_error.clear();
     if (!info) return fail(SK_ERR_INVALID_ARG, "info is NULL");
     sk::LinearAttnPlan lp;
-    sk_status s = linear_plan(B, T, H, dk, dv, num_segments, opts, &lp);
+    int path = 0;
+    sk_status s = linear_plan(B, T, H, dk, dv, num_segments, opts, &lp, &path);
     if (s != SK_OK) return s;
     memset(info, 0, sizeof *info);
     info->num_segments = lp.N;
     info->segment_len = lp.L;
     info->workspace_bytes = lp.ws_bytes;
     info->launches = lp.N > 1 ? 3 : 1;
+    info->path = path;
     return SK_OK;
 }
 
@@ -496,7 +518,8 @@ sk_status sk_linear_attn_fwd(const void* q, const void* k, const void* v, const 
     if (!(di.major == 10 && di.minor == 3))
         return fail(SK_ERR_UNSUPPORTED, "this library runs on sm_103 (GB300) only");
     sk::LinearAttnPlan lp;
-    s = linear_plan(B, T, H, dk, dv, num_segments, opts, &lp);
+    int path = 0;
+    s = linear_plan(B, T, H, dk, dv, num_segments, opts, &lp, &path);
     if (s != SK_OK) return s;
     if (T == 0) return SK_OK;
     if (!q || !k || !v || !g || !out || !workspace) return fail(SK_ERR_INVALID_ARG, "NULL pointer");
@@ -509,7 +532,18 @@ sk_status sk_linear_attn_fwd(const void* q, const void* k, const void* v, const 
     if (opts && opts->event_begin &&
         (e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_begin), stream)) != cudaSuccess)
         return fail_cuda(e, "cudaEventRecord");
-    e = launch_linear_attn(lp, q, k, v, g, out, workspace, scale, stream);
+    if (path == SK_PATH_LINEAR_CHUNK) {
+        const uint64_t timeout_ns =
+            uint64_t(opts && opts->wait_timeout_us > 0 ? opts->wait_timeout_us : 2000000) * 1000ull;
+        CUtensorMap tmQ, tmK, tmV, tmG;
+        const long long rows = (long long)B * T;
+        if (!make_kv_map(&tmQ, q, H, kLinearAttnDim, rows) || !make_kv_map(&tmK, k, H, kLinearAttnDim, rows) ||
+            !make_kv_map(&tmV, v, H, kLinearAttnDim, rows) || !make_g_map(&tmG, g, H, rows))
+            return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (linear attention)");
+        e = launch_linear_attn_tc(lp, tmQ, tmK, tmV, tmG, q, k, v, g, out, workspace, scale, timeout_ns, stream);
+    } else {
+        e = launch_linear_attn(lp, q, k, v, g, out, workspace, scale, stream);
+    }
     if (e != cudaSuccess) return fail_cuda(e, "linear attention launch");
     if (opts && opts->event_end &&
         (e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), stream)) != cudaSuccess)
@@ -558,6 +592,6 @@ const char* sk_attn_status_string(sk_status s) {
 
 const char* sk_attn_last_error(void) { return g_last_error.c_str(); }
 
-int sk_attn_version(void) { return 102; }
+int sk_attn_version(void) { return 103; }
 
 }  // extern "C"

@@ -378,4 +378,13 @@ cudaError_t launch_linear_attn(const LinearAttnPlan& lp, const void* q, const vo
     return cudaGetLastError();
 }
 
+cudaError_t launch_linear_combine(const LinearAttnPlan& lp, void* workspace, cudaStream_t stream) {
+    LaParams p = {};
+    p.hs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.hs_off);
+    p.logm = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.logm_off);
+    p.B = lp.B; p.T = lp.T; p.H = lp.H; p.N = lp.N; p.L = lp.L;
+    gla_combine_kernel<<<dim3(kD * kD / 256, lp.H, lp.B), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace sk

@@ -1,13 +1,16 @@
 // linear_attn.h -- host plan and launcher of the chunk-parallel gated linear
 // attention (linear_attn.cu).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 namespace sk {
 
 constexpr int kLinearAttnDim = 128;        // dk = dv
-constexpr int kLinearAttnMinSegment = 64;  // tokens per segment when the count is chosen
+constexpr int kLinearAttnMinSegment = 64;        // tokens per segment when the count is chosen (recurrent)
+constexpr int kLinearAttnMinSegmentChunk = 128;  // the same for the tensor-core windows
 
 struct LinearAttnPlan {
     int B = 0, T = 0, H = 0;
@@ -18,8 +21,9 @@ struct LinearAttnPlan {
 
 // Segments: n_req > 0 asks for that many (at most T); 0 fills one wave of SMs
 // with (segment, head, sequence) CTAs while every segment keeps at least
-// kLinearAttnMinSegment tokens.  Empty trailing segments are dropped.
-inline void make_linear_attn_plan(int B, int T, int H, int n_req, int sms, LinearAttnPlan* p) {
+// min_segment tokens.  Empty trailing segments are dropped.
+inline void make_linear_attn_plan(int B, int T, int H, int n_req, int sms, LinearAttnPlan* p,
+                                  int min_segment = kLinearAttnMinSegment) {
     p->B = B;
     p->T = T;
     p->H = H;
@@ -27,7 +31,7 @@ inline void make_linear_attn_plan(int B, int T, int H, int n_req, int sms, Linea
     if (n <= 0) {
         const long long bh = (long long)B * H;
         n = bh >= sms ? 1 : sms / bh;
-        const long long by_len = (T + kLinearAttnMinSegment - 1) / kLinearAttnMinSegment;
+        const long long by_len = (T + min_segment - 1) / min_segment;
         if (n > by_len) n = by_len;
     }
     if (n > T) n = T;
@@ -42,7 +46,21 @@ inline void make_linear_attn_plan(int B, int T, int H, int n_req, int sms, Linea
 
 size_t linear_attn_smem_segment();
 size_t linear_attn_smem_output();
+size_t linear_attn_tc_smem();
+// Token-by-token passes on the FMA pipes (linear_attn.cu).
 cudaError_t launch_linear_attn(const LinearAttnPlan& lp, const void* q, const void* k, const void* v,
                                const float* g, void* out, void* workspace, float scale, cudaStream_t stream);
+// Window passes on the tensor cores (linear_attn_tc.cu); bounded waits report
+// through the workspace's status word.
+// q, k, v also come as 2-D maps [B * T][H * 128] (boxes of 128 rows x 64 columns,
+// 128-byte swizzle) and g as a 2-D fp32 map of the same shape (boxes of 128 x 128,
+// no swizzle) for the window copies.
+cudaError_t launch_linear_attn_tc(const LinearAttnPlan& lp, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                  const CUtensorMap& tmV, const CUtensorMap& tmG, const void* q, const void* k,
+                                  const void* v,
+                                  const float* g, void* out, void* workspace, float scale, uint64_t timeout_ns,
+                                  cudaStream_t stream);
+// The affine combine over the segments' (log M, h) in the workspace (both paths).
+cudaError_t launch_linear_combine(const LinearAttnPlan& lp, void* workspace, cudaStream_t stream);
 
 }  // namespace sk

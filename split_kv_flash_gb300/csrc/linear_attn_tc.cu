@@ -23,12 +23,13 @@
 // stays fp32 in TMEM across windows; only its copy St for the window's first
 // product is rounded to bf16.
 //
-// One CTA per (segment, head, sequence); 160 threads: warps 0-3 own TMEM lanes
-// 0-127 (thread i: key channel i for the operands and the state, token row i
-// of A and O); a window's q, k, v rows arrive by TMA in the operand
-// tiles' layout and are turned into the decayed operands in place, its log
-// decays by TMA as a row-major fp32 block; warp 4 issues the MMAs from one
-// elected lane.  Every wait is bounded.
+// One CTA per (segment, head, sequence); 288 threads: warps 0-7 are operand
+// warps (TMEM lane i % 128 is key channel i % 128 of the state and token row
+// i % 128 of the scores and outputs; its two threads take 64 columns each),
+// warp 8 issues the MMAs from one elected lane.  A window's q, k, v rows
+// arrive by TMA in the operand tiles' layout and are turned into the decayed
+// operands in place; its log decays arrive by TMA as a row-major fp32 block.
+// Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -42,7 +43,9 @@ namespace sk {
 namespace {
 
 constexpr int kD = kLinearAttnDim;  // 128 = dk = dv = window rows
-constexpr int kTcThreads = 160;
+constexpr int kMathWarps = 8;         // operand / softmax-free elementwise warps; warp 8 issues the MMAs
+constexpr int kMathThreads = 32 * kMathWarps;
+constexpr int kTcThreads = kMathThreads + 32;
 constexpr int kTile = kD * kD * 2;   // one 128 x 128 bf16 operand tile, two 64-column SW128 chunks
 constexpr int kOffQ = 0;             // Qt [t][i]
 constexpr int kOffK = kTile;         // Kt [s][i]
@@ -51,7 +54,7 @@ constexpr int kOffV = 3 * kTile;     // V  [s][j]
 constexpr int kOffA = 4 * kTile;     // mask(A) [t][s]
 constexpr int kOffS = 5 * kTile;     // St [i][j]
 constexpr int kOffMisc = 6 * kTile;  // window ends, barriers, TMEM address, flags
-constexpr int kSmemTc = kOffMisc + 1024 + 1024;  // + misc + alignment slack
+constexpr int kSmemTc = kOffMisc + 3072 + 1024;  // + misc + alignment slack
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kWindowRange = 60.f;  // largest range of b inside a window of more than one token
 constexpr float kLogDecayClamp = 100.f;
@@ -77,10 +80,6 @@ struct LaTcParams {
     int clear_status;  // 1 on the call's first launch: CTA (0, 0, 0) zeroes the status word
 };
 
-__device__ __forceinline__ unsigned short bf16_bits(float x) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    return *reinterpret_cast<const unsigned short*>(&h);
-}
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -130,27 +129,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sKh = base + kOffKh, sV = base + kOffV;
     const uint32_t sA = base + kOffA, sS = base + kOffS;
     int* wmin = reinterpret_cast<int*>(smem + kOffMisc);          // [4] per-warp window ends
+    float* cs = reinterpret_cast<float*>(smem + kOffMisc + 1024);  // [128] window centre c per channel
+    float* ehs = cs + kD;                                          // [128] e^{b_end - c} per channel
+    float* bnd = cs + 2 * kD;                                      // [128] b_end per channel
     volatile int* win_n = reinterpret_cast<volatile int*>(smem + kOffMisc + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 20);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc + 24);
     const uint32_t bars = base + kOffMisc + 64;
     const uint32_t bar_op = bars, bar_at = bars + 8, bar_a = bars + 16, bar_o = bars + 24, bar_s = bars + 32,
-                   bar_drain = bars + 40, bar_ld = bars + 48;
+                   bar_drain = bars + 40, bar_ld = bars + 48, bar_ldv = bars + 56;
 
     if (threadIdx.x == 0) {
         if (p.clear_status && seg == 0 && h == 0 && b == 0) *p.status = 0u;
-        mbar_init(bar_op, 128);
-        mbar_init(bar_at, 128);
+        mbar_init(bar_op, kMathThreads);
+        mbar_init(bar_at, kMathThreads);
         mbar_init(bar_a, 1);
         mbar_init(bar_o, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_drain, 1);
         mbar_init(bar_ld, 1);
+        mbar_init(bar_ldv, 1);
         *abort_flag = 0;
         *win_n = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kMathWarps) {
         tmem_alloc(smem_u32(tmem_holder), 512);
         tmem_relinquish();
     }
@@ -167,30 +170,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tA = tmem, tO = tmem + 128, tS = tmem + 256;  // A, O, S: 128 columns each
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
-    if (warp < 4) {
-        // ===================== operand warps: thread i = key channel / TMEM lane i
+    if (warp < kMathWarps) {
+        // ===================== operand warps.  TMEM lane li = i % 128 belongs to
+        // warps w and w + 4 (lane quarter w % 4); thread i takes the 64 columns
+        // [64 half, 64 half + 64) of lane li's rows (half = i / 128).  The scans
+        // over the rows of a key channel run in the threads of half 0.
         const int i = threadIdx.x;
-        const uint32_t lane_off = uint32_t(32 * warp) << 16;
-        const size_t tok = size_t(p.H) * kD;                              // elements between tokens
+        const int li = i & 127, half = i >> 7;
+        const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+        const size_t tok = size_t(p.H) * kD;  // elements between tokens
 
         // The state in TMEM: S_in(s) (output pass, s > 0) or zero.
         {
-            const float* src = (OUT && seg > 0) ? p.hs + ((size_t(seg) * p.B + b) * p.H + h) * kD * kD + size_t(i) * kD
-                                                : nullptr;
+            const float* src = (OUT && seg > 0)
+                                   ? p.hs + ((size_t(seg) * p.B + b) * p.H + h) * kD * kD + size_t(li) * kD + 64 * half
+                                   : nullptr;
 #pragma unroll
-            for (int c = 0; c < kD / 16; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 float x[16];
 #pragma unroll
                 for (int e = 0; e < 16; e += 4) {
                     float4 v4 = src ? *reinterpret_cast<const float4*>(src + c * 16 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
                     x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
                 }
-                tmem_st16(tS + lane_off + c * 16, x);
+                tmem_st16(tS + lane_off + 64 * half + c * 16, x);
             }
             tmem_wait_st();
         }
 
-        float gsum = 0.f;  // segment pass: log M_s of channel i
+        // A window's copies: q (output pass), k and g, whose tiles free up once the
+        // window's scores and output products are done, and v, whose tile frees
+        // up with the state update; each set is issued as soon as its tiles are
+        // free (the next window's start is known by then).
+        const uint64_t pol = l2_policy_evict_first();
+        auto issue_qkg = [&](int ustart) {
+            const int row = b * p.T + ustart;
+            mbar_arrive_expect_tx(bar_ld, uint32_t((OUT ? 2 : 1) * kTile + kD * kD * 4));
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                tma_load_2d(sK + cc * 16384, &tmK, bar_ld, h * kD + cc * 64, row, pol);
+                if (OUT) tma_load_2d(sQ + cc * 16384, &tmQ, bar_ld, h * kD + cc * 64, row, pol);
+            }
+            tma_load_2d(sA, &tmG, bar_ld, h * kD, row, pol);
+        };
+        auto issue_v = [&](int ustart) {
+            const int row = b * p.T + ustart;
+            mbar_arrive_expect_tx(bar_ldv, uint32_t(kTile));
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) tma_load_2d(sV + cc * 16384, &tmV, bar_ldv, h * kD + cc * 64, row, pol);
+        };
+        if (i == 0 && t0 < t1) {
+            issue_qkg(t0);
+            issue_v(t0);
+        }
+
+        float gsum = 0.f;  // segment pass: log M_s of channel li (half 0)
         int u0 = t0;
         // The loop's control flow depends on nothing a wait returns: a wait that
         // gives up raises the abort flag, every later wait returns at once, and
@@ -203,121 +237,165 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive(bar_op);
                 break;
             }
-            // ---- the window's 128 rows of q, k, v by TMA (raw, into the operand
-            // tiles, transformed in place below) and of g (fp32, row-major, into
-            // the mask(A) and St tiles, free until the products need them); the
-            // previous window's products have all completed (bar_s).
-            if (i == 0) {
-                const uint64_t pol = l2_policy_evict_first();
-                const int row = b * p.T + u0;
-                mbar_arrive_expect_tx(bar_ld, uint32_t((OUT ? 3 : 2) * kTile + kD * kD * 4));
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    tma_load_2d(sK + cc * 16384, &tmK, bar_ld, h * kD + cc * 64, row, pol);
-                    tma_load_2d(sV + cc * 16384, &tmV, bar_ld, h * kD + cc * 64, row, pol);
-                    if (OUT) tma_load_2d(sQ + cc * 16384, &tmQ, bar_ld, h * kD + cc * 64, row, pol);
-                }
-                tma_load_2d(sA, &tmG, bar_ld, h * kD, row, pol);
-            }
+            // ---- the window's 128 rows of q, k (raw, into the operand tiles,
+            // transformed in place below), g (fp32, row-major, into the mask(A)
+            // and St tiles, free until the products need them) and v, by TMA
             mbar_wait(bar_ld, w & 1, wc, (kKernLinear << 8) | kSiteLinLoad);
-            const float* gs = reinterpret_cast<const float*>(smem + kOffA) + i;  // g of row r: gs[r * kD]
-            // ---- window end: before the first token that widens a channel's range
-            // of b beyond kWindowRange (the window's first token always counts)
+            // ---- running sums b_r of channel li over the 128 rows, in place of g,
+            // and the window end: before the first token that widens a channel's
+            // range of b beyond kWindowRange (the window's first token always
+            // counts).  The range max - min of the running sums never shrinks, so
+            // the rows before the first violation are those where it is in bounds.
             const int cap = min(u0 + kD, t1);
-            // the range mx - mn of the running sums never shrinks, so the rows
-            // before the first violation are those where it is still in bounds
-            int end;
-            {
+            float* gs = reinterpret_cast<float*>(smem + kOffA) + li;  // g of row r: gs[r * kD]
+            float mx_all = 0.f, mn_all = 0.f;                          // over the rows before cap
+            if (half == 0) {
                 float cum = 0.f, mx = 0.f, mn = 0.f;
                 int in_range = 0;
-#pragma unroll 8
+#pragma unroll 16
                 for (int r = 0; r < kD; ++r) {
                     cum += clamp_g(gs[r * kD]);
-                    mx = fmaxf(mx, cum);
-                    mn = fminf(mn, cum);
-                    in_range += (r == 0 || mx - mn <= kWindowRange) ? 1 : 0;
-                }
-                end = min(u0 + in_range, cap);
-            }
-            end = __reduce_min_sync(0xffffffffu, end);
-            if (lane == 0) wmin[warp] = end;
-            named_bar_sync(1, 128);
-            const int u1 = min(min(wmin[0], wmin[1]), min(wmin[2], wmin[3]));
-            const int n = u1 - u0;
-            // ---- the window's range of b for channel i: centre c and end value
-            float bend = 0.f, c = 0.f;
-            {
-                float cum = 0.f, mx = 0.f, mn = 0.f;
-#pragma unroll 8
-                for (int r = 0; r < kD; ++r) {
-                    const float gr = clamp_g(gs[r * kD]);
-                    if (r < n) {
-                        cum += gr;
+                    gs[r * kD] = cum;
+                    if (u0 + r < cap) {
                         mx = fmaxf(mx, cum);
                         mn = fminf(mn, cum);
                     }
+                    in_range += (r == 0 || mx - mn <= kWindowRange) ? 1 : 0;
                 }
-                bend = cum;
-                c = 0.5f * (mx + mn);
+                mx_all = mx;
+                mn_all = mn;
+                int end = min(u0 + in_range, cap);
+                end = __reduce_min_sync(0xffffffffu, end);
+                if (lane == 0) wmin[warp] = end;
             }
-            gsum += bend;
-            // ---- operands in place, row r = token u0 + r; rows past the window are
-            // zero.  Rows go in batches of 16 whose raw q, k and g are read first,
-            // so the shared-memory loads of a batch are in flight together.
-            {
-                unsigned short* tQ = reinterpret_cast<unsigned short*>(smem + kOffQ);
-                unsigned short* tK = reinterpret_cast<unsigned short*>(smem + kOffK);
-                unsigned short* tKh = reinterpret_cast<unsigned short*>(smem + kOffKh);
-                unsigned short* tV = reinterpret_cast<unsigned short*>(smem + kOffV);
-                // element (row r, column i) of a 128 x 128 bf16 tile of two 64-column SW128
-                // chunks: chunk i / 64, then row r, 16-byte granule (i % 64) / 8 swizzled by r
-                const uint32_t o0 = uint32_t(i >> 6) * 16384u + uint32_t(i & 7) * 2u;
-                const int gi = (i & 63) >> 3;
-                const float ehc = fast_exp2((bend - c) * kLog2e);
-                float cum = 0.f;
-#pragma unroll 1
-                for (int r0 = 0; r0 < kD; r0 += 16) {
-                    unsigned short kraw[16], qraw[16];
-                    float gr[16];
+            named_bar_sync(1, kMathThreads);
+            const int u1 = min(min(wmin[0], wmin[1]), min(wmin[2], wmin[3]));
+            const int n = u1 - u0;
+            // ---- the window's range of b for channel li (0 included): centre c,
+            // end value; when no channel cut the window short it is the range above
+            if (half == 0) {
+                const float bend = gs[(n - 1) * kD];
+                float mx = mx_all, mn = mn_all;
+                if (u1 < cap) {
+                    float mx8[8], mn8[8];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        const uint32_t o = (o0 + sw128_offset(r0 + r, gi)) >> 1;
-                        kraw[r] = tK[o];
-                        if constexpr (OUT) qraw[r] = tQ[o];
-                        gr[r] = clamp_g(gs[(r0 + r) * kD]);
-                    }
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        const uint32_t o = (o0 + sw128_offset(r0 + r, gi)) >> 1;
-                        const bool in = r0 + r < n;
-                        cum += in ? gr[r] : 0.f;
-                        const float ek = fast_exp2((c - cum) * kLog2e);  // e^{c - b}
-                        const float kv = __uint_as_float(uint32_t(kraw[r]) << 16);
-                        tKh[o] = in ? bf16_bits(kv * (ek * ehc)) : (unsigned short)0;  // e^{b_end - b}
-                        if constexpr (OUT) {
-                            const float qv = __uint_as_float(uint32_t(qraw[r]) << 16);
-                            tQ[o] = in ? bf16_bits(qv * fast_exp2((cum - c) * kLog2e)) : (unsigned short)0;
-                            tK[o] = in ? bf16_bits(kv * ek) : (unsigned short)0;
+                    for (int e = 0; e < 8; ++e) mx8[e] = mn8[e] = 0.f;
+#pragma unroll 16
+                    for (int r = 0; r < kD; ++r) {
+                        const float b_r = gs[r * kD];
+                        if (r < n) {
+                            mx8[r & 7] = fmaxf(mx8[r & 7], b_r);
+                            mn8[r & 7] = fminf(mn8[r & 7], b_r);
                         }
-                        if (!in) tV[o] = 0;
+                    }
+                    mx = mx8[0];
+                    mn = mn8[0];
+#pragma unroll
+                    for (int e = 1; e < 8; ++e) {
+                        mx = fmaxf(mx, mx8[e]);
+                        mn = fminf(mn, mn8[e]);
                     }
                 }
+                const float c = 0.5f * (mx + mn);
+                gsum += bend;
+                cs[li] = c;
+                ehs[li] = fast_exp2((bend - c) * kLog2e);
+                bnd[li] = bend;
             }
-            named_bar_sync(1, 128);  // every thread is done with g before St overwrites it
-            if constexpr (OUT) {
-                // St row i = e^{c} P[i][:] (P: the state before the window, in TMEM)
-                const float ec = fast_exp2(c * kLog2e);
+            named_bar_sync(1, kMathThreads);
+            // ---- operands in place, row r = token u0 + r; rows past the window are
+            // zero.  Here a thread takes 8 channels (one 16-byte granule of a row,
+            // cg = i % 16) of rows i / 16 + 16 m: 16-byte shared accesses.
+            {
+                const int cg = i & 15, rsub = i >> 4;
+                float c8[8], eh8[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int e = 0; e < 8; ++e) {
+                    c8[e] = cs[8 * cg + e];
+                    eh8[e] = ehs[8 * cg + e];
+                }
+                const uint32_t chunk = uint32_t(cg >> 3) * 16384u;
+                const float* brow = reinterpret_cast<const float*>(smem + kOffA) + 8 * cg;
+#pragma unroll 2
+                for (int m = 0; m < kD / 16; ++m) {
+                    const int r = rsub + 16 * m;
+                    const uint32_t off = chunk + sw128_offset(r, cg & 7);
+                    const bool in = r < n;
+                    uint4 kraw, qraw = make_uint4(0u, 0u, 0u, 0u);
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(kraw.x), "=r"(kraw.y), "=r"(kraw.z), "=r"(kraw.w) : "r"(sK + off));
+                    if constexpr (OUT)
+                        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(qraw.x), "=r"(qraw.y), "=r"(qraw.z), "=r"(qraw.w) : "r"(sQ + off));
+                    const float4 b0 = *reinterpret_cast<const float4*>(brow + r * kD);
+                    const float4 b1 = *reinterpret_cast<const float4*>(brow + r * kD + 4);
+                    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                    const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
+                    const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+                    uint32_t oh[4], ok_[4], oq[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        float kh[2], kt[2], qt[2];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int e = 2 * e2 + h2;
+                            const float kv = __uint_as_float(h2 ? (kw[e2] & 0xFFFF0000u) : (kw[e2] << 16));
+                            const float ek = fast_exp2((c8[e] - bv[e]) * kLog2e);  // e^{c - b}
+                            kh[h2] = kv * (ek * eh8[e]);                            // k e^{b_end - b}
+                            kt[h2] = kv * ek;
+                            if constexpr (OUT) {
+                                const float qv = __uint_as_float(h2 ? (qw[e2] & 0xFFFF0000u) : (qw[e2] << 16));
+                                qt[h2] = qv * fast_exp2((bv[e] - c8[e]) * kLog2e);  // q e^{b - c}
+                            } else {
+                                qt[h2] = 0.f;
+                            }
+                        }
+                        oh[e2] = in ? pack_bf16x2(kh[0], kh[1]) : 0u;
+                        ok_[e2] = in ? pack_bf16x2(kt[0], kt[1]) : 0u;
+                        oq[e2] = in ? pack_bf16x2(qt[0], qt[1]) : 0u;
+                    }
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sKh + off), "r"(oh[0]), "r"(oh[1]),
+                                 "r"(oh[2]), "r"(oh[3]) : "memory");
+                    if constexpr (OUT) {
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sK + off), "r"(ok_[0]),
+                                     "r"(ok_[1]), "r"(ok_[2]), "r"(ok_[3]) : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sQ + off), "r"(oq[0]),
+                                     "r"(oq[1]), "r"(oq[2]), "r"(oq[3]) : "memory");
+                    }
+                }
+                // v rows past the window: zero (0 x Inf would be NaN in the products)
+                mbar_wait(bar_ldv, w & 1, wc, (kKernLinear << 8) | kSiteLinLoad);
+#pragma unroll 2
+                for (int m = 0; m < kD / 16; ++m) {
+                    const int r = rsub + 16 * m;
+                    if (r >= n)
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sV + chunk + sw128_offset(r, cg & 7)),
+                                     "r"(0u)
+                                     : "memory");
+                }
+            }
+            named_bar_sync(1, kMathThreads);  // every thread is done with g before St overwrites it
+            const float bend_l = bnd[li];
+            if constexpr (!OUT) {
+                // the raw k and g of this window are consumed: the next window's come now
+                if (i == 0 && u0 + n < t1) issue_qkg(u0 + n);
+            }
+            if constexpr (OUT) {
+                // St row li = e^{c} P[li][:] (P: the state before the window, in TMEM)
+                const float ec = fast_exp2(cs[li] * kLog2e);
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int q = 2 * half + q2;
                     float x[32];
                     tmem_ld32(tS + lane_off + q * 32, x);
-                    store_row32_bf16(sS, i, q, x, ec);
+                    store_row32_bf16(sS, li, q, x, ec);
                 }
             } else {
                 // segment pass: scale the state now (no product reads it before MMA_S)
-                const float e = fast_exp2(bend * kLog2e);
+                const float e = fast_exp2(bend_l * kLog2e);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int q = 2 * half + q2;
                     float x[32];
                     tmem_ld32(tS + lane_off + q * 32, x);
 #pragma unroll
@@ -333,22 +411,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(bar_op);
 
             if constexpr (OUT) {
-                // ---- mask(A) row t = i: keep s <= t; then scale the state
+                // ---- mask(A) row t = li: keep s <= t; then scale the state
                 mbar_wait(bar_a, w & 1, wc, (kKernLinear << 8) | kSiteLinScores);
                 tc_fence_after();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int q = 2 * half + q2;
                     float x[32];
                     tmem_ld32(tA + lane_off + q * 32, x);
 #pragma unroll
                     for (int e4 = 0; e4 < 32; ++e4)
-                        if (q * 32 + e4 > i) x[e4] = 0.f;
-                    store_row32_bf16(sA, i, q, x, 1.f);
+                        if (q * 32 + e4 > li) x[e4] = 0.f;
+                    store_row32_bf16(sA, li, q, x, 1.f);
                 }
                 {
-                    const float e = fast_exp2(bend * kLog2e);
+                    const float e = fast_exp2(bend_l * kLog2e);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const int q = 2 * half + q2;
                         float x[32];
                         tmem_ld32(tS + lane_off + q * 32, x);
 #pragma unroll
@@ -361,16 +441,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar_at);
-                // ---- outputs of the window: token row t = i of O
+                // ---- outputs of the window: token row t = li of O, this thread's 64
+                // value columns straight to global memory.  The TMEM loads are
+                // warp-collective: every lane takes part, only the window's rows
+                // are stored.
                 mbar_wait(bar_o, w & 1, wc, (kKernLinear << 8) | kSiteLinOut);
                 tc_fence_after();
-                // O row t = i (all 128 value columns) straight to global memory.  The
-                // TMEM loads are warp-collective: every lane takes part, only the
-                // rows of the window are stored.
+                // the scores and output products are done with Qt, Kt, mask(A), St
+                if (i == 0 && u0 + n < t1) issue_qkg(u0 + n);
                 {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t(b) * p.T + u0 + i) * tok + size_t(h) * kD);
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t(b) * p.T + u0 + li) * tok + size_t(h) * kD);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const int q = 2 * half + q2;
                         float x[32];
                         tmem_ld32(tO + lane_off + q * 32, x);
 #pragma unroll
@@ -380,30 +463,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             v4.y = pack_bf16x2(x[8 * g8 + 2] * p.scale, x[8 * g8 + 3] * p.scale);
                             v4.z = pack_bf16x2(x[8 * g8 + 4] * p.scale, x[8 * g8 + 5] * p.scale);
                             v4.w = pack_bf16x2(x[8 * g8 + 6] * p.scale, x[8 * g8 + 7] * p.scale);
-                            if (i < n) dst[4 * q + g8] = v4;
+                            if (li < n) dst[4 * q + g8] = v4;
                         }
                     }
                 }
             }
             mbar_wait(bar_s, w & 1, wc, (kKernLinear << 8) | kSiteLinState);
             tc_fence_after();
+            if (i == 0 && u0 + n < t1) issue_v(u0 + n);  // the state update is done with V
             u0 += n;
         }
         if constexpr (!OUT) {
             // h_s (the end state from zero) and log M_s
-            float* dst = p.hs + ((size_t(seg) * p.B + b) * p.H + h) * kD * kD + size_t(i) * kD;
+            float* dst = p.hs + ((size_t(seg) * p.B + b) * p.H + h) * kD * kD + size_t(li) * kD + 64 * half;
 #pragma unroll
-            for (int cc = 0; cc < kD / 16; ++cc) {
+            for (int cc = 0; cc < 4; ++cc) {
                 float x[16];
-                tmem_ld16(tS + lane_off + cc * 16, x);
+                tmem_ld16(tS + lane_off + 64 * half + cc * 16, x);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
                     *reinterpret_cast<float4*>(dst + cc * 16 + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
             }
-            p.logm[((size_t(seg) * p.B + b) * p.H + h) * kD + i] = gsum;
+            if (half == 0) p.logm[((size_t(seg) * p.B + b) * p.H + h) * kD + li] = gsum;
         }
-    } else if (warp == 4) {
+    } else if (warp == kMathWarps) {
         // ===================== MMA issuer (the whole warp runs the loop)
         const bool leader = elect_one();
         // K-major operand: rows = M (or N) index, 64-column chunks of K; a K step
@@ -468,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, 512);
+    if (warp == kMathWarps) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace

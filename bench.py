@@ -624,9 +624,20 @@ def linear_flops(w):
 ALU_FP32_TFLOPS_PER_SM_GHZ = 128 * 2 / 1e3  # FP32 FMA lanes per SM x 2 flops, TFLOP/s per GHz
 
 
-def gpu_linear(sk, device, clock_mhz, reps=10):
-    """Lone calls (L2 flushed before each) at the planned segment count and, for
-    the speedup the issue reports, with one segment per (sequence, head)."""
+def linear_tensor_flops(w, N, L):
+    """MMA work of the chunk path: per window of at most 128 tokens, four
+    128 x 128 x 128 products in the output pass and one in the segment pass
+    (segments 0 .. N-2); full windows when the decays do not cut them short."""
+    per = 2.0 * 128 ** 3
+    wins = [-(-min(L, w.T - s * L) // 128) for s in range(N)]
+    return w.B * w.H * per * (4 * sum(wins) + sum(wins[:-1]))
+
+
+def gpu_linear(sk, device, clock_mhz, bf16_peak, reps=10):
+    """Lone calls (L2 flushed before each) of the default (tensor-core window)
+    path at the planned segment count and, for the speedup the issue reports,
+    with one segment per (sequence, head); and of the token-by-token path at the
+    planned segment count."""
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -640,19 +651,25 @@ def gpu_linear(sk, device, clock_mhz, reps=10):
         v = torch.randn(shape, device=device, generator=g_).to(torch.bfloat16)
         g = -w.gmax * torch.rand(shape, device=device, generator=g_)
         row = {"workload": w.name}
-        for tag, n in (("", 0), ("one_segment_", 1)):
-            info = sk.sk_linear_attn_plan(w.B, w.T, w.H, num_segments=n)
-            out, ws = sk.linear_attn_fwd(q, k, v, g, w.scale, n)
+        for tag, n, path in (("", 0, sk.SK_PATH_LINEAR_CHUNK), ("one_segment_", 1, sk.SK_PATH_LINEAR_CHUNK),
+                             ("recurrent_", 0, sk.SK_PATH_LINEAR_RECURRENT)):
+            o = sk.Opts()
+            o.force_path = path
+            info = sk.sk_linear_attn_plan(w.B, w.T, w.H, num_segments=n, opts=o)
+            out, ws = sk.linear_attn_fwd(q, k, v, g, w.scale, n, opts=o)
             ms = []
             for i in range(reps):
                 flush.fill_(float(i))
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                sk.linear_attn_fwd(q, k, v, g, w.scale, n, out=out, workspace=ws, stream=stream)
+                sk.linear_attn_fwd(q, k, v, g, w.scale, n, out=out, workspace=ws, stream=stream, opts=o)
                 e1.record(stream)
                 torch.cuda.synchronize(device)
                 ms.append(e0.elapsed_time(e1))
+            st, where = sk.sk_attn_workspace_status(ws)
+            if st != 0:
+                raise RuntimeError("linear attention: device status %d at %d (%s)" % (st, where, w.name))
             m = statistics.median(ms)
             row[tag + "us"] = m * 1e3
             row[tag + "segments"] = info.num_segments
@@ -660,7 +677,10 @@ def gpu_linear(sk, device, clock_mhz, reps=10):
                 row["tokens_per_s"] = w.B * w.T * w.H / (m * 1e-3)
                 row["tflops"] = linear_flops(w) / (m * 1e-3) / 1e12
                 row["frac_of_alu_peak"] = row["tflops"] / alu_peak
+                row["tensor_tflops"] = linear_tensor_flops(w, info.num_segments, info.segment_len) / (m * 1e-3) / 1e12
+                row["frac_of_bf16_peak"] = row["tensor_tflops"] / bf16_peak
         row["speedup_vs_one_segment"] = row["one_segment_us"] / row["us"]
+        row["speedup_vs_recurrent"] = row["recurrent_us"] / row["us"]
         rows.append(row)
         del q, k, v, g, out, ws
     return rows, alu_peak
@@ -913,12 +933,17 @@ def main():
                       "bytes = latent rows once + Q + O + LSE",
             **latent_summary(lrows)}
         result["latent_rows"] = lrows
-        lin, alu_peak = gpu_linear(sk, device, clocks.get("sm_mhz") or 2070.0)
+        lin, alu_peak = gpu_linear(sk, device, clocks.get("sm_mhz") or 2070.0, bf16_peak)
         result["linear"] = {
-            "unit": "us per call (L2 flushed), tokens x heads per s, TFLOP/s and fraction of the FP32 FMA peak",
-            "bound": "alu", "peak_tflops": alu_peak,
-            "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x the SM clock sampled during the run",
-            "flop_count": "5 dk dv per token and head (state update 3, output 2)",
+            "unit": "us per call (L2 flushed), tokens x heads per s, TFLOP/s and fractions of the FP32 FMA and "
+                    "bf16 tensor peaks",
+            "path": "tensor-core windows (the default); recurrent_us: the token-by-token FMA path",
+            "bound": "tensor", "peak_tflops": bf16_peak, "alu_peak_tflops": alu_peak,
+            "peak_source": "measured bf16 burst; ALU: 152 SMs x 128 FP32 lanes x 2 flops x the SM clock "
+                           "sampled during the run",
+            "flop_count": "tflops: 5 dk dv per token and head (the recurrence's work); tensor_tflops: the "
+                          "window products, 4 x 2 x 128^3 per window of the output pass and 2 x 128^3 per "
+                          "window of the segment pass",
             **{r["workload"].replace("gla_", "") + "_" + k: (round(v, 4) if isinstance(v, float) else v)
                for r in lin for k, v in r.items() if k != "workload"}}
         result["host_us_per_call"] = host_cost_us(sk, device)

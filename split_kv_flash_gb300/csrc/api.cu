@@ -540,7 +540,8 @@ sk_status sk_linear_attn_fwd(const void* q, const void* k, const void* v, const 
         if (!make_kv_map(&tmQ, q, H, kLinearAttnDim, rows) || !make_kv_map(&tmK, k, H, kLinearAttnDim, rows) ||
             !make_kv_map(&tmV, v, H, kLinearAttnDim, rows) || !make_g_map(&tmG, g, H, rows))
             return fail(SK_ERR_CUDA, "cuTensorMapEncodeTiled failed (linear attention)");
-        e = launch_linear_attn_tc(lp, tmQ, tmK, tmV, tmG, q, k, v, g, out, workspace, scale, timeout_ns, stream);
+        e = launch_linear_attn_tc(lp, tmQ, tmK, tmV, tmG, q, k, v, g, out, workspace, scale, timeout_ns,
+                                  opts ? opts->debug_inject_stall : 0, stream);
     } else {
         e = launch_linear_attn(lp, q, k, v, g, out, workspace, scale, stream);
     }

@@ -59,7 +59,7 @@ cudaError_t launch_linear_attn_tc(const LinearAttnPlan& lp, const CUtensorMap& t
                                   const CUtensorMap& tmV, const CUtensorMap& tmG, const void* q, const void* k,
                                   const void* v,
                                   const float* g, void* out, void* workspace, float scale, uint64_t timeout_ns,
-                                  cudaStream_t stream);
+                                  int inject_stall, cudaStream_t stream);
 // The affine combine over the segments' (log M, h) in the workspace (both paths).
 cudaError_t launch_linear_combine(const LinearAttnPlan& lp, void* workspace, cudaStream_t stream);
 

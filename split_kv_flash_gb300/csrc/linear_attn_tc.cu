@@ -78,6 +78,7 @@ struct LaTcParams {
     int B, T, H, N, L;
     float scale;
     int clear_status;  // 1 on the call's first launch: CTA (0, 0, 0) zeroes the status word
+    int inject_stall;  // test hook: the MMA warp first waits on a barrier nothing signals
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc + 24);
     const uint32_t bars = base + kOffMisc + 64;
     const uint32_t bar_op = bars, bar_at = bars + 8, bar_a = bars + 16, bar_o = bars + 24, bar_s = bars + 32,
-                   bar_drain = bars + 40, bar_ld = bars + 48, bar_ldv = bars + 56;
+                   bar_drain = bars + 40, bar_ld = bars + 48, bar_ldv = bars + 56, bar_never = bars + 64;
 
     if (threadIdx.x == 0) {
         if (p.clear_status && seg == 0 && h == 0 && b == 0) *p.status = 0u;
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bar_drain, 1);
         mbar_init(bar_ld, 1);
         mbar_init(bar_ldv, 1);
+        mbar_init(bar_never, 1);
         *abort_flag = 0;
         *win_n = 0;
         fence_mbar_init();
@@ -503,6 +505,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         constexpr uint32_t id_km = make_idesc_bf16(128, 128, false, true);
         constexpr uint32_t id_mm = make_idesc_bf16(128, 128, true, true);
         bool ok = true;
+        if (p.inject_stall) {
+            // gives up first (half the limit), so the status names this wait
+            const WaitCtl wc_half{wc.abort_flag, wc.status, wc.limit_ns / 2};
+            ok = mbar_wait(bar_never, 0, wc_half, (kKernLinear << 8) | kSiteInjected);
+            ok = __all_sync(0xffffffffu, ok);
+        }
         for (int w = 0;; ++w) {
             ok = mbar_wait(bar_op, w & 1, wc, (kKernLinear << 8) | kSiteLinOperands) && ok;
             ok = __all_sync(0xffffffffu, ok);
@@ -563,7 +571,7 @@ cudaError_t launch_linear_attn_tc(const LinearAttnPlan& lp, const CUtensorMap& t
                                   const CUtensorMap& tmV, const CUtensorMap& tmG, const void* q, const void* k,
                                   const void* v,
                                   const float* g, void* out, void* workspace, float scale, uint64_t timeout_ns,
-                                  cudaStream_t stream) {
+                                  int inject_stall, cudaStream_t stream) {
     (void)q;
     (void)k;
     (void)v;
@@ -574,6 +582,7 @@ cudaError_t launch_linear_attn_tc(const LinearAttnPlan& lp, const CUtensorMap& t
     p.logm = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.logm_off);
     p.status = static_cast<uint32_t*>(workspace);
     p.timeout_ns = timeout_ns;
+    p.inject_stall = inject_stall;
     p.B = lp.B; p.T = lp.T; p.H = lp.H; p.N = lp.N; p.L = lp.L;
     p.scale = scale;
     cudaError_t e;

@@ -211,3 +211,24 @@ def test_latent_fwd_without_gpu_fails_cleanly(sk):
     with pytest.raises(sk.SKError) as ei:
         sk.sk_attn_fwd_latent(16, 16, 16, 16, 1, 16, 2, [256], 576, 512, 0.07, 1, -1, 256, 1 << 20)
     assert ei.value.status in (2, 5)
+
+
+def test_linear_plan_paths_without_gpu(sk):
+    """The linear-attention planner picks the window path by default, the
+    recurrent path on request, and rejects attention paths; the window path asks
+    for at least 128 tokens per segment, the recurrent one for 64."""
+    o = _opts(sk, num_sms=152)
+    info = sk.sk_linear_attn_plan(1, 8192, 4, opts=o)
+    assert info.path == sk.SK_PATH_LINEAR_CHUNK and info.num_segments == 38 and info.launches == 3
+    o = _opts(sk, num_sms=152, force_path=sk.SK_PATH_LINEAR_RECURRENT)
+    info = sk.sk_linear_attn_plan(1, 8192, 4, opts=o)
+    assert info.path == sk.SK_PATH_LINEAR_RECURRENT and info.num_segments == 38
+    # short sequence: the minimum segment length decides the count
+    short = {}
+    for path in (sk.SK_PATH_LINEAR_CHUNK, sk.SK_PATH_LINEAR_RECURRENT):
+        short[path] = sk.sk_linear_attn_plan(1, 1000, 4, opts=_opts(sk, num_sms=152, force_path=path))
+    assert short[sk.SK_PATH_LINEAR_CHUNK].num_segments == 8      # ceil(1000 / 128)
+    assert short[sk.SK_PATH_LINEAR_RECURRENT].num_segments == 16  # ceil(1000 / 64)
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_linear_attn_plan(1, 64, 1, opts=_opts(sk, num_sms=152, force_path=sk.SK_PATH_PREFILL))
+    assert ei.value.status == 1

@@ -146,3 +146,20 @@ def test_force_path_rejects_attention_paths(sk):
     with pytest.raises(sk.SKError) as ei:
         sk.sk_linear_attn_plan(1, 64, 1, opts=o)
     assert ei.value.status == 1
+
+
+def test_injected_stall_times_out_and_recovers(sk):
+    """Failure detection of the window path without a GPU fault: one MMA-warp
+    wait targets a barrier nothing signals; it gives up after half the 20 ms
+    limit, the kernels finish, the status word names that wait, and a correct
+    call on the same workspace follows."""
+    w = wl.linear_attn(1, 512, 2)
+    q, k, v, g = [t.cuda() for t in wl.make_linear_inputs(w)]
+    o = _opts(sk, CHUNK)
+    o.debug_inject_stall = 1
+    o.wait_timeout_us = 20000
+    out, ws = sk.linear_attn_fwd(q, k, v, g, w.scale, 2, opts=o)
+    st, where = sk.sk_attn_workspace_status(ws)
+    assert st == 6  # SK_ERR_DEVICE_TIMEOUT
+    assert where == (3 << 8) | 8  # linear-attention kernel, the injected wait
+    _check(sk, w, 2, path=CHUNK)

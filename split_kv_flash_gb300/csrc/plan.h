@@ -18,6 +18,13 @@ constexpr int kMaxSplits = 128;         // the combine kernel merges at most 128
 // Decode path: a split must save at least this many 128-key blocks of one CTA's
 // time to pay for the combine kernel (about 2.2 us against 0.75-0.8 us a block).
 constexpr int kDecodeCombineBlocks = 3;
+// Split choice by list schedule (sequences of different lengths): a CTA's fixed
+// cost in 128-key blocks (set-up, first copies, epilogue: ~3 us against 0.75 us
+// a block), the cost of a CTA past its sequence's splits, and the largest grid
+// that is simulated.
+constexpr double kCtaOverheadBlocks = 4.0;
+constexpr double kCtaEmptyBlocks = 0.3;
+constexpr long long kScheduleMaxCtas = 16384;
 
 // Shared-memory rings of the decode kernel (K and V slots of 128 rows), also
 // needed by the scheduler: the in-kernel merge stages a tile's partials there.

@@ -133,7 +133,9 @@ def test_forced_split_counts_match_oracle(sk):
 
 def test_fill_policy_invariants(sk):
     """The default policy (own, measured choice): splits tile each range exactly,
-    every CTA fits in one wave when splitting, and no split repeats a chunk."""
+    every CTA fits in one wave when splitting (unless sequences of different
+    lengths on the decode path chose a multi-wave count by list schedule), and no
+    split repeats a chunk."""
     for num_sms in (148, 152):
         for (B, Hq, Hkv, sq, kv, d, causal, window) in _cases():
             o = _opts(sk, 0, num_sms)
@@ -143,7 +145,9 @@ def test_fill_policy_invariants(sk):
             assert info.num_splits == max(sb)
             if info.needs_combine:
                 ctas = sum(c * info.head_tiles * info.num_m_blocks for c in sb)
-                assert ctas <= num_sms
+                if ctas > num_sms:
+                    assert B > 1 and len(set(kv)) > 1 and info.path == sk.SK_PATH_DECODE
+                    assert S in (2, 4, 8, 16)
                 if info.path == sk.SK_PATH_DECODE:
                     # a split pays for the combine only when it saves 3 blocks
                     nblk = po.ceil_div(max(kv), 128)
@@ -163,6 +167,45 @@ def test_short_verify_keeps_one_split(sk):
         info = sk.sk_attn_plan(2, 16, 16, 9, [kv] * 2, 128, True, -1, _opts(sk, 0, 152))
         assert info.path == sk.SK_PATH_DECODE
         assert bool(info.needs_combine) == split, kv
+
+
+def _list_schedule(table, sms, overhead=4.0, empty=0.3):
+    """Finishing time (in KV blocks) of the CTAs of a plan table taken in launch
+    order by the first free SM."""
+    import heapq
+    free = [0.0] * sms
+    end = 0.0
+    for lo, hi, _word, work in table:
+        t = heapq.heappop(free)
+        t += (hi - lo + overhead) if work else empty
+        end = max(end, t)
+        heapq.heappush(free, t)
+    return end
+
+
+def test_varlen_decode_split_count_by_list_schedule(sk):
+    """Decode of 16 sequences of different lengths on 152 SMs: one wave (the
+    fill policy gives one split) leaves the longest sequences streaming alone,
+    so the planner takes a multi-wave split count, the one among 1, 2, 4, 8, 16
+    whose list schedule (recomputed here from the oracle's per-CTA ranges)
+    finishes first, by more than 3 % where it differs from one split."""
+    import workloads as wl
+    w = wl.varlen_decode(16)
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, 1, w.kv_len, 128, opts=_opts(sk, 0, 152))
+    S = info.num_splits_policy
+    assert S > 1 and info.num_ctas > 152
+    G = w.Hq // w.Hkv
+    times = {}
+    for c in (1, 2, 4, 8, 16):
+        sb = po.split_counts(w.kv_len, 128, c)
+        table = po.cta_table(1, w.kv_len, G, bool(info.pack_gqa), info.head_tiles, info.kBlockM, 128,
+                             info.num_m_blocks, max(sb), sb, False, -1)
+        times[c] = _list_schedule(table, 152)
+    assert times[S] <= min(times.values()) / 0.97 + 1e-9
+    assert times[S] < 0.97 * times[1]
+    # equal lengths keep one wave
+    info = sk.sk_attn_plan(4, 32, 8, 1, [20000] * 4, 128, opts=_opts(sk, 0, 152))
+    assert info.num_ctas <= 152
 
 
 def test_gqa_decode_split_counts(sk):

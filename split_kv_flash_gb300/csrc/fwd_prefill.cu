@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sk = seqs.seq_len(b);
     const int kv_off = seqs.seq_off(b);
     const BlockRange br =
-        tile_key_blocks(p.sq, sk, tc.m_block, p.kBlockM, p.kBlockN, p.win, p.pack_gqa ? p.G : 1, word);
+        tile_key_blocks(p.sq, sk, tc.m_block, 128 * kHalves, 128, p.win, p.pack_gqa ? p.G : 1, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
     const int kvh = p.pack_gqa ? ht : ht / p.G;
     const int m0 = tc.m_block * (128 * kHalves);
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < kHalves; ++t) {
         rows_h[t] = max(0, min(128, p.rows - (m0 + 128 * t)));
-        const BlockRange hr = tile_key_blocks(p.sq, sk, tc.m_block * kHalves + t, 128, p.kBlockN, p.win,
+        const BlockRange hr = tile_key_blocks(p.sq, sk, tc.m_block * kHalves + t, 128, 128, p.win,
                                               p.pack_gqa ? p.G : 1, split_word(0, 1));
         const int lo = max(hr.lo, br.lo), hi = min(hr.hi, br.hi);
         count[t] = (rows_h[t] > 0 && hi > lo) ? hi - lo : 0;

@@ -32,6 +32,7 @@
 
 #include "fwd_common.cuh"
 #include "linear_attn.h"
+#include "sm103_ptx.cuh"
 
 namespace sk {
 namespace {
@@ -306,6 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) gla_segment_kernel(const __grid_c
 __global__ void __launch_bounds__(256) gla_combine_kernel(const __grid_constant__ LaParams p) {
     const int e = blockIdx.x * 256 + threadIdx.x;   // element of the 128 x 128 state
     const int h = blockIdx.y, b = blockIdx.z;
+    // Launched as a programmatic dependent of the segment pass: let the output
+    // pass be scheduled, then wait for the segment pass's states.
+    griddep_launch_dependents();
+    griddep_wait();
     const int row = e / kD;
     const size_t stride = size_t(p.B) * p.H * kD * kD;   // between segments
     float* hp = p.hs + (size_t(b) * p.H + h) * kD * kD + e;
@@ -383,8 +388,8 @@ cudaError_t launch_linear_combine(const LinearAttnPlan& lp, void* workspace, cud
     p.hs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.hs_off);
     p.logm = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.logm_off);
     p.B = lp.B; p.T = lp.T; p.H = lp.H; p.N = lp.N; p.L = lp.L;
-    gla_combine_kernel<<<dim3(kD * kD / 256, lp.H, lp.B), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(reinterpret_cast<const void*>(gla_combine_kernel), dim3(kD * kD / 256, lp.H, lp.B), dim3(256),
+                      0, stream, p);
 }
 
 }  // namespace sk

@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The next kernel on the stream (the combine, or the output pass) may be
+    // scheduled now; it waits for this grid's completion before it reads.
+    griddep_launch_dependents();
     const uint32_t tmem = *tmem_holder;
     const uint32_t tA = tmem, tO = tmem + 128, tS = tmem + 256;  // A, O, S: 128 columns each
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
@@ -182,28 +185,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
         const size_t tok = size_t(p.H) * kD;  // elements between tokens
 
-        // The state in TMEM: S_in(s) (output pass, s > 0) or zero.
-        {
-            const float* src = (OUT && seg > 0)
-                                   ? p.hs + ((size_t(seg) * p.B + b) * p.H + h) * kD * kD + size_t(li) * kD + 64 * half
-                                   : nullptr;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float x[16];
-#pragma unroll
-                for (int e = 0; e < 16; e += 4) {
-                    float4 v4 = src ? *reinterpret_cast<const float4*>(src + c * 16 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
-                }
-                tmem_st16(tS + lane_off + 64 * half + c * 16, x);
-            }
-            tmem_wait_st();
-        }
-
-        // A window's copies: q (output pass), k and g, whose tiles free up once the
-        // window's scores and output products are done, and v, whose tile frees
-        // up with the state update; each set is issued as soon as its tiles are
-        // free (the next window's start is known by then).
+        // The first window's copies: the inputs are not written by the kernel
+        // this grid may overlap (the combine), so they go before the wait below.
         const uint64_t pol = l2_policy_evict_first();
         auto issue_qkg = [&](int ustart) {
             const int row = b * p.T + ustart;
@@ -225,7 +208,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             issue_qkg(t0);
             issue_v(t0);
         }
+        // The incoming states are the previous kernel's output.
+        griddep_wait();
 
+        // The state in TMEM: S_in(s) (output pass, s > 0) or zero.
+        {
+            const float* src = (OUT && seg > 0)
+                                   ? p.hs + ((size_t(seg) * p.B + b) * p.H + h) * kD * kD + size_t(li) * kD + 64 * half
+                                   : nullptr;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; e += 4) {
+                    float4 v4 = src ? *reinterpret_cast<const float4*>(src + c * 16 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
+                }
+                tmem_st16(tS + lane_off + 64 * half + c * 16, x);
+            }
+            tmem_wait_st();
+        }
+
+        // Later windows' copies: q (output pass), k and g, whose tiles free up once
+        // a window's scores and output products are done, and v, whose tile frees
+        // up with the state update; each set is issued as soon as its tiles are
+        // free (the next window's start is known by then).
         float gsum = 0.f;  // segment pass: log M_s of channel li (half 0)
         int u0 = t0;
         // The loop's control flow depends on nothing a wait returns: a wait that
@@ -596,6 +603,9 @@ cudaError_t launch_linear_attn_tc(const LinearAttnPlan& lp, const CUtensorMap& t
         p.clear_status = 0;
         if ((e = launch_linear_combine(lp, workspace, stream)) != cudaSuccess) return e;
     }
+    if (lp.N > 1)  // a programmatic dependent of the combine: its first copies overlap the combine
+        return launch_pdl(reinterpret_cast<const void*>(gla_tc_kernel<true>), dim3(lp.N, lp.H, lp.B),
+                          dim3(kTcThreads), kSmemTc, stream, p, tmQ, tmK, tmV, tmG);
     gla_tc_kernel<true><<<dim3(lp.N, lp.H, lp.B), kTcThreads, kSmemTc, stream>>>(p, tmQ, tmK, tmV, tmG);
     return cudaGetLastError();
 }

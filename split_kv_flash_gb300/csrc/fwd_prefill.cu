@@ -109,27 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<int4*>(p.echo + cta_lin * 4) = make_int4(0, 0, int(word), 0);
         return;
     }
-    const int sk = seqs.seq_len(b);
-    const int kv_off = seqs.seq_off(b);
-    const BlockRange br =
-        tile_key_blocks(p.sq, sk, tc.m_block, 128 * kHalves, 128, p.win, p.pack_gqa ? p.G : 1, word);
-    const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
-    const int kvh = p.pack_gqa ? ht : ht / p.G;
     const int m0 = tc.m_block * (128 * kHalves);
-
-    // Each half's own block range (section 3.2 applied to its 128 rows), clipped
-    // to the CTA's split share.  Visiting step j (block br.hi - 1 - j) belongs to
-    // half t for j in [first[t], first[t] + count[t]).
-    int first[kHalves], count[kHalves], rows_h[kHalves];
-#pragma unroll
-    for (int t = 0; t < kHalves; ++t) {
-        rows_h[t] = max(0, min(128, p.rows - (m0 + 128 * t)));
-        const BlockRange hr = tile_key_blocks(p.sq, sk, tc.m_block * kHalves + t, 128, 128, p.win,
-                                              p.pack_gqa ? p.G : 1, split_word(0, 1));
-        const int lo = max(hr.lo, br.lo), hi = min(hr.hi, br.hi);
-        count[t] = (rows_h[t] > 0 && hi > lo) ? hi - lo : 0;
-        first[t] = count[t] > 0 ? br.hi - hi : 0;
-    }
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::kOffQ;
@@ -150,17 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_k = [&](int s) { return sbase + C::kOffK + uint32_t(s) * C::kKBytes; };
     auto stage_v = [&](int s) { return sbase + C::kOffV + uint32_t(s) * C::kVBytes; };
 
-    if (warp == 2 && lane == 0 && nblocks > 0 && p.q_tma) {
-        // While the CTA sets up: the tile's Q into L2, marked evict-first like
-        // its copies below (read once; K/V, re-read by other tiles, keep L2).
-        // Only a hint; global writes land in L2, so the copies after the grid
-        // dependency below still read current data.
-        for (int t = 0; t < kHalves; ++t)
-#pragma unroll
-            for (int c = 0; c < HD / 64; ++c)
-                tma_prefetch_l2_4d_hint(&tmQ, c * 64, 0, ht, b * p.sq + (m0 + 128 * t) / p.q_gp,
-                                        l2_policy_evict_first());
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < KST; ++s) {
             mbar_init(bar_kfull(s), 1);
@@ -180,7 +149,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        if (p.q_tma) {
+            // The tile's Q halves go out first, before the block ranges below are
+            // worked out.  Q may be the previous kernel's output: wait for it.
+            griddep_wait();
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) {
+                mbar_arrive_expect_tx(bar_qfull(t), C::kQBytes);
+                const int qrow = b * p.sq + (m0 + 128 * t) / p.q_gp;
+#pragma unroll
+                for (int c = 0; c < HD / 64; ++c)
+                    tma_load_4d(sQ + uint32_t(t * C::kQBytes + c * 16384), &tmQ, bar_qfull(t), c * 64, 0, ht, qrow,
+                                l2_policy_evict_first());
+            }
+        }
     }
+    const int sk = seqs.seq_len(b);
+    const int kv_off = seqs.seq_off(b);
+    const BlockRange br =
+        tile_key_blocks(p.sq, sk, tc.m_block, 128 * kHalves, 128, p.win, p.pack_gqa ? p.G : 1, word);
+    const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
+    const int kvh = p.pack_gqa ? ht : ht / p.G;
+
+    // Each half's own block range (section 3.2 applied to its 128 rows), clipped
+    // to the CTA's split share.  Visiting step j (block br.hi - 1 - j) belongs to
+    // half t for j in [first[t], first[t] + count[t]).
+    int first[kHalves], count[kHalves], rows_h[kHalves];
+#pragma unroll
+    for (int t = 0; t < kHalves; ++t) {
+        rows_h[t] = max(0, min(128, p.rows - (m0 + 128 * t)));
+        const BlockRange hr = tile_key_blocks(p.sq, sk, tc.m_block * kHalves + t, 128, 128, p.win,
+                                              p.pack_gqa ? p.G : 1, split_word(0, 1));
+        const int lo = max(hr.lo, br.lo), hi = min(hr.hi, br.hi);
+        count[t] = (rows_h[t] > 0 && hi > lo) ? hi - lo : 0;
+        first[t] = count[t] > 0 ? br.hi - hi : 0;
+    }
+
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
         tmem_relinquish();
@@ -206,20 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtl wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
-        // ===================== producer: Q halves, then the K/V rings
+        // ===================== producer: the K/V rings (thread 0 issued the Q halves)
         const bool leader = elect_one();
-        if (p.q_tma && leader) {
-#pragma unroll
-            for (int t = 0; t < kHalves; ++t) {
-                mbar_arrive_expect_tx(bar_qfull(t), C::kQBytes);
-                const int qrow = b * p.sq + (m0 + 128 * t) / p.q_gp;
-#pragma unroll
-                for (int c = 0; c < HD / 64; ++c)
-                    tma_load_4d(sQ + uint32_t(t * C::kQBytes + c * 16384), &tmQ, bar_qfull(t), c * 64, 0, ht, qrow,
-                                l2_policy_evict_first());
-            }
-        }
-        __syncwarp();
         // K/V of one head are re-read by the other m blocks: keep them in L2.
         const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
         const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};

@@ -141,15 +141,6 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x
                  : "memory");
 }
 
-// One tile of a 4-D tensor map into L2 with an L2 eviction policy (a hint, as above).
-__device__ __forceinline__ void tma_prefetch_l2_4d_hint(const CUtensorMap* map, int c0, int c1, int c2, int c3,
-                                                        uint64_t l2_policy) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3, %4}], %5;" ::"l"(
-                     map),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(l2_policy)
-                 : "memory");
-}
-
 // One tile of a 2-D tensor map into L2 (a hint: no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)

@@ -170,6 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_key_blocks(p.sq, sk, tc.m_block, 128 * kHalves, 128, p.win, p.pack_gqa ? p.G : 1, word);
     const int nblocks = br.hi > br.lo ? br.hi - br.lo : 0;
     const int kvh = p.pack_gqa ? ht : ht / p.G;
+    // The first K block (the last of the range: blocks are visited downwards)
+    // follows the Q halves at once, into slot 0 of the K ring (free at start).
+    const bool k0_early = p.q_tma && nblocks > 0;
+    if (threadIdx.x == 0 && k0_early) {
+        mbar_arrive_expect_tx(bar_kfull(0), C::kKBytes);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+            tma_load_2d(stage_k(0) + c * 16384, &tmK, bar_kfull(0), kvh * HD + c * 64, kv_off + (br.hi - 1) * 128,
+                        l2_policy_evict_last());
+    }
 
     // Each half's own block range (section 3.2 applied to its 128 rows), clipped
     // to the CTA's split share.  Visiting step j (block br.hi - 1 - j) belongs to
@@ -215,8 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K/V of one head are re-read by the other m blocks: keep them in L2.
         const KvRing kr{stage_k(0), uint32_t(C::kKBytes), bar_kfull(0), bar_kempty(0), KST};
         const KvRing vr{stage_v(0), uint32_t(C::kVBytes), bar_vfull(0), bar_vempty(0), VST};
-        produce_kv<HD>(&tmK, &tmV, kr, vr, nblocks, kvh * HD, kv_off + br.lo * 128, true, l2_policy_evict_last(),
-                       wc, (kKernPrefill << 8) | kSiteProducerEmpty, leader);
+        int kpos = 0, vpos = 0;
+        produce_kv_tile<HD>(&tmK, &tmV, kr, vr, 0, nblocks, kvh * HD, kv_off + br.lo * 128, true,
+                            l2_policy_evict_last(), wc, (kKernPrefill << 8) | kSiteProducerEmpty, leader, kpos, vpos,
+                            k0_early);
+        drain_ring(kr, kpos, wc.limit_ns);
+        drain_ring(vr, vpos, wc.limit_ns);
         // Q copies land before the CTA exits (the MMA waited for them unless it gave up).
         if (p.q_tma)
             for (int t = 0; t < kHalves; ++t) mbar_drain(bar_qfull(t), 0, wc.limit_ns);

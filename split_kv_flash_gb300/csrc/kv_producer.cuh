@@ -47,16 +47,16 @@ __device__ __forceinline__ bool load_block(const CUtensorMap* tm, const KvRing& 
 }
 
 // K and V blocks of rows y0 + 128 * visit_block(j), j in [0, nblocks), into
-// ring positions g0 + j.  kpos / vpos advance past every load issued, so the
+// ring positions g0 + j (K of j = 0 skipped when the caller has issued it).  kpos / vpos advance past every load issued, so the
 // caller can drain exactly those; returns false once a wait has given up.
 template <int HD>
 __device__ __forceinline__ bool produce_kv_tile(const CUtensorMap* tmK, const CUtensorMap* tmV, const KvRing& K,
                                                 const KvRing& V, int g0, int nblocks, int x0, int y0, bool desc,
                                                 uint64_t policy, const WaitCtl& wc, int where, bool leader,
-                                                int& kpos, int& vpos) {
+                                                int& kpos, int& vpos, bool k0_issued = false) {
     auto row = [&](int j) { return y0 + visit_block(j, nblocks, desc) * 128; };
     if (nblocks > 0) {
-        if (!load_block<HD>(tmK, K, g0, x0, row(0), policy, wc, where, leader)) return false;
+        if (!k0_issued && !load_block<HD>(tmK, K, g0, x0, row(0), policy, wc, where, leader)) return false;
         kpos = g0 + 1;
     }
     for (int j = 1; j <= nblocks; ++j) {

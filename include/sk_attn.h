@@ -232,8 +232,10 @@ sk_status sk_attn_fwd_latent(const void* q, const void* kv, void* out, float* ls
  *     segments' h_ext / incoming states and log M); q, k, v, g, out 16-byte
  *     aligned.  Same error rules as sk_attn_fwd.  The chunk path's device waits
  *     are bounded by opts->wait_timeout_us; one that gives up leaves its code in
- *     the workspace's status word (sk_attn_workspace_status), which the call's
- *     first kernel clears.  The state is never returned. */
+ *     the workspace's status word (sk_attn_workspace_status).  On both paths the
+ *     call's first kernel clears that word, so the workspace needs no zero fill
+ *     (the token-by-token path has no bounded wait and leaves it at zero).  The
+ *     state is never returned. */
 typedef struct {
     int num_segments;        /* N actually used */
     int segment_len;         /* L */

@@ -52,8 +52,10 @@ struct LaParams {
     __nv_bfloat16* out;
     float* hs;     // [N][B][H][dk][dv]: h_s, then (after the combine) S_in(s)
     float* logm;   // [N][B][H][dk]
+    uint32_t* status;  // workspace header word: this path has no bounded wait, so it only clears it
     int B, T, H, N, L;
     float scale;
+    int clear_status;  // 1 on the call's first launch: CTA (0, 0, 0) zeroes the status word
 };
 
 // Shared-memory staging of one chunk: fp32 k, exp(g), v and (output pass) q.
@@ -281,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_segment_kernel(const __grid_c
     Stage& st = *reinterpret_cast<Stage*>(smem_raw);
     float* gred = reinterpret_cast<float*>(smem_raw + sizeof(Stage));  // [16][128]
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    if (p.clear_status && s == 0 && h == 0 && b == 0 && threadIdx.x == 0) *p.status = 0u;
     const int t0 = s * p.L, t1 = min(p.T, (s + 1) * p.L);
     float S[kS];
 #pragma unroll
@@ -342,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) gla_output_kernel(const __grid_co
     Stage& st = *reinterpret_cast<Stage*>(smem_raw);
     auto osm = reinterpret_cast<__nv_bfloat16(*)[kD]>(smem_raw + sizeof(Stage));
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    if (p.clear_status && s == 0 && h == 0 && b == 0 && threadIdx.x == 0) *p.status = 0u;
     const int t0 = s * p.L, t1 = min(p.T, (s + 1) * p.L);
     float S[kS];
 #pragma unroll
@@ -366,8 +370,10 @@ cudaError_t launch_linear_attn(const LinearAttnPlan& lp, const void* q, const vo
     p.out = static_cast<__nv_bfloat16*>(out);
     p.hs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.hs_off);
     p.logm = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lp.logm_off);
+    p.status = static_cast<uint32_t*>(workspace);
     p.B = lp.B; p.T = lp.T; p.H = lp.H; p.N = lp.N; p.L = lp.L;
     p.scale = scale;
+    p.clear_status = 1;
     const int smem_a = int(linear_attn_smem_segment()), smem_c = int(linear_attn_smem_output());
     cudaError_t e;
     if ((e = ensure_smem_attr(reinterpret_cast<const void*>(gla_segment_kernel), smem_a)) != cudaSuccess ||
@@ -376,6 +382,7 @@ cudaError_t launch_linear_attn(const LinearAttnPlan& lp, const void* q, const vo
     if (lp.N > 1) {
         gla_segment_kernel<<<dim3(lp.N - 1, lp.H, lp.B), kThreads, smem_a, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        p.clear_status = 0;
         gla_combine_kernel<<<dim3(kD * kD / 256, lp.H, lp.B), 256, 0, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -163,3 +163,20 @@ def test_injected_stall_times_out_and_recovers(sk):
     assert st == 6  # SK_ERR_DEVICE_TIMEOUT
     assert where == (3 << 8) | 8  # linear-attention kernel, the injected wait
     _check(sk, w, 2, path=CHUNK)
+
+
+@pytest.mark.parametrize("nseg", [1, 3])
+@pytest.mark.parametrize("path", PATHS)
+def test_call_clears_stale_status_word(sk, nseg, path):
+    """The workspace header word reports a wait that gave up during the call;
+    whatever it held before (an earlier call's report, reused memory) the
+    call's first launch clears it, on both paths and segment layouts."""
+    w = wl.linear_attn(1, 384, 2)
+    q, k, v, g = [t.cuda() for t in wl.make_linear_inputs(w)]
+    o = _opts(sk, path)
+    info = sk.sk_linear_attn_plan(w.B, w.T, w.H, num_segments=nseg, opts=o)
+    ws = torch.full((max(int(info.workspace_bytes), 256),), 0xA5, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(v)
+    sk.linear_attn_fwd(q, k, v, g, w.scale, nseg, out=out, workspace=ws, opts=o)
+    st, where = sk.sk_attn_workspace_status(ws)
+    assert (st, where) == (0, 0)

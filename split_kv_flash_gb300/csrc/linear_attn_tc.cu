@@ -280,6 +280,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             named_bar_sync(1, kMathThreads);
             const int u1 = min(min(wmin[0], wmin[1]), min(wmin[2], wmin[3]));
             const int n = u1 - u0;
+            if (i == kMathThreads - 1 && u1 < t1) {
+                // The next window starts at u1: its rows into L2 now, so that its
+                // copies, issued once this window's products free the tiles, hit L2.
+                const int row = b * p.T + u1;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    tma_prefetch_l2_2d(&tmK, h * kD + cc * 64, row);
+                    tma_prefetch_l2_2d(&tmV, h * kD + cc * 64, row);
+                    if (OUT) tma_prefetch_l2_2d(&tmQ, h * kD + cc * 64, row);
+                }
+                tma_prefetch_l2_2d(&tmG, h * kD, row);
+            }
             // ---- the window's range of b for channel li (0 included): centre c,
             // end value; when no channel cut the window short it is the range above
             if (half == 0) {

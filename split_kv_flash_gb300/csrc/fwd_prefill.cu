@@ -411,10 +411,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_mask = (blk_last >= sk) || (has_causal && blk_last > diag_lo) ||
                                    (has_window && blk_first < diag_hi - p.window_left) || rows_valid < 128;
             if (need_mask) {
+                // A diagonal block cuts its rows above (c_hi), a block at the
+                // window's left edge below (c_lo); the warp takes the one-sided
+                // test unless one of its rows needs both.
                 const int c_lo = key_lo - blk_first, c_hi = key_hi - blk_first;
+                const bool cut_hi = __any_sync(0xffffffffu, c_hi < 127);
+                const bool cut_lo = __any_sync(0xffffffffu, c_lo > 0);
+                if (cut_hi && cut_lo) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+                    for (int c = 0; c < 128; ++c)
+                        if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+                } else if (cut_hi) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c > c_hi) x[c] = -INFINITY;
+                } else if (cut_lo) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c < c_lo) x[c] = -INFINITY;
+                }
             }
             // Row max: 8 chains of 16 columns, two columns per three-input max.
             float mx8[8];

@@ -511,11 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (stage && cnt == 0 && p.q_tma) {
             mbar_wait(bar_qfull(t), 0, wc, (kKernPrefill << 8) | kSiteMmaQ);
         }
+        // O row read from TMEM 64 columns per wait, then scaled and written 16 at a time.
+        float o64[64];
 #pragma unroll
         for (int c = 0; c < HD / 16; ++c) {
-            float o[16];
-            if (cnt >= 1) {
-                tmem_ld16(tO(t) + lane_off + c * 16, o);
+            float* o = o64 + 16 * (c & 3);
+            if ((c & 3) == 0 && cnt >= 1) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) tmem_ld16(tO(t) + lane_off + (c + u) * 16, o64 + 16 * u);
                 tmem_wait_ld();
             }
 #pragma unroll

@@ -554,17 +554,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[3] = make_float4(o[12], o[13], o[14], o[15]);
                 }
             }
-        }
-        if (stage) {
-            fence_proxy_async_smem();
-            named_bar_sync(2 + t, 128);  // the half's 128 threads
-            if (sidx == 0) {
-#pragma unroll
-                for (int c = 0; c < HD / 64; ++c)
-                    tma_store_5d(&tmO, sQt + uint32_t(c * 16384), c * 64, 0, ht, (m0 + 128 * t) / p.q_gp, b);
-                bulk_commit_group();
-                bulk_wait_group_read0();  // the source stays valid until the copy has read it
+            if (stage && (c & 3) == 3) {
+                // 64 columns of the half's rows are staged: their TMA store goes
+                // out while the next 64 are written.
+                fence_proxy_async_smem();
+                named_bar_sync(2 + t, 128);  // the half's 128 threads
+                if (sidx == 0)
+                    tma_store_5d(&tmO, sQt + uint32_t((c >> 2) * 16384), (c >> 2) * 64, 0, ht,
+                                 (m0 + 128 * t) / p.q_gp, b);
             }
+        }
+        if (stage && sidx == 0) {
+            bulk_commit_group();
+            bulk_wait_group_read0();  // the source stays valid until the copies have read it
         }
         if (row_ok) {
             if (final_out)

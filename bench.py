@@ -917,6 +917,11 @@ def main():
             pre[key + "_frac_of_bf16_peak"] = tf / bf16_peak
         pre["traffic"] = ncu_traffic("prefill_causal_8192", PREFILL_SOURCES)
         result["prefill"] = pre
+        # The same figures as top-level scalars, for readers that keep only those.
+        for key in ("causal", "local1024"):
+            result["prefill_%s_tflops" % key] = pre[key + "_tflops"]
+            result["prefill_%s_ms" % key] = pre[key + "_ms"]
+            result["prefill_%s_frac" % key] = pre[key + "_frac_of_bf16_peak"]
     if rank == 0 and not args.no_sweep:
         rows = gpu_sweep(sk, device, hbm_peak)
         result["sweep"] = {

@@ -64,8 +64,10 @@ SK_HD uint32_t split_word(int split_idx, int split_count) {
 // `group` > 1 the rows are packed: row r is query position r / group.
 SK_HD BlockRange tile_key_blocks(int q_len, int kv_len, int tile, int tile_rows, int block_keys,
                                  const KeyWindow& w, int group, uint32_t word) {
-    const int first_q = (tile * tile_rows) / group;
-    const int last_q = imin((tile * tile_rows + tile_rows - 1) / group, q_len - 1);
+    // (group 1 and one split are the common case: no integer division there)
+    const int first_q = group == 1 ? tile * tile_rows : (tile * tile_rows) / group;
+    const int last_q =
+        imin(group == 1 ? tile * tile_rows + tile_rows - 1 : (tile * tile_rows + tile_rows - 1) / group, q_len - 1);
     const int shift = kv_len - q_len;  // query i's diagonal key is i + shift
     int begin = 0;
     int end = div_up(kv_len, block_keys);
@@ -80,7 +82,7 @@ SK_HD BlockRange tile_key_blocks(int q_len, int kv_len, int tile, int tile_rows,
     if (end <= begin) return {0, 0};
     const int count = int(word >> 16);
     const int idx = int(word & 0xFFFF);
-    const int share = div_up(end - begin, count);
+    const int share = count == 1 ? end - begin : div_up(end - begin, count);
     const int lo = begin + idx * share;
     const int hi = imin(lo + share, end);
     if (hi <= lo) return {0, 0};
@@ -100,8 +102,8 @@ SK_HD TileCoord tile_of_cta(int bx, int by, int bz, int num_m_blocks, int num_sp
                             bool reverse_m) {
     TileCoord t;
     t.m_block = reverse_m ? (num_m_blocks - 1 - bx) : bx;
-    t.head_tile = by / num_splits;
-    t.split = by % num_splits;
+    t.head_tile = num_splits == 1 ? by : by / num_splits;
+    t.split = num_splits == 1 ? 0 : by % num_splits;
     t.batch = bz;
     return t;
 }

@@ -103,6 +103,20 @@ typedef enum {
                                     per CTA */
 } sk_prefill_schedule;
 
+/* How the decode kernel's grid maps to tiles when the sequences of a batch have
+ * different split counts (sk_attn_opts.tile_map; tiling chapter section 4.5,
+ * the varlen scheduler's warp prefix sum over per-sequence tile counts). */
+typedef enum {
+    SK_TILE_MAP_AUTO = 0,    /* the library chooses (currently the grid) */
+    SK_TILE_MAP_GRID = 1,    /* grid (m blocks, head tiles x grid splits, sequences); a CTA whose
+                                split index is past its sequence's split count exits at once */
+    SK_TILE_MAP_PACKED = 2   /* one-dimensional grid over the CTAs that have work, in the grid's
+                                order without the empty ones: sequence b owns head_tiles x
+                                splits_b x num_m_blocks consecutive CTAs, and each CTA finds its
+                                sequence by a warp prefix sum over the split counts.  Decode path,
+                                batches of more than one sequence with different split counts */
+} sk_tile_map;
+
 /* Options; an all-zero struct (or NULL) selects the defaults. */
 typedef struct {
     int policy;            /* sk_split_policy */
@@ -119,6 +133,7 @@ typedef struct {
     void* event_end;       /* optional cudaEvent_t recorded just after it */
     int combine_mode;      /* sk_combine_mode */
     int prefill_schedule;  /* sk_prefill_schedule */
+    int tile_map;          /* sk_tile_map */
 } sk_attn_opts;
 
 /* The host scheduler's decisions for one problem. */
@@ -133,7 +148,8 @@ typedef struct {
     int num_splits;           /* grid splits = max over sequences of the per-sequence count */
     int num_splits_policy;    /* the count the policy chose before per-sequence sizing */
     int num_n_blocks_max;     /* ceil(max kv_len / kBlockN) */
-    int grid_x, grid_y, grid_z; /* partial kernel grid: (num_m_blocks, head_tiles*num_splits, B) */
+    int grid_x, grid_y, grid_z; /* partial kernel grid: (num_m_blocks, head_tiles*num_splits, B), or
+                                   (num_ctas, 1, 1) with the packed tile map */
     long long num_ctas;       /* grid_x * grid_y * grid_z */
     int needs_combine;        /* 1: some sequence has more than one split */
     size_t workspace_bytes;   /* bytes of device workspace sk_attn_fwd needs */
@@ -146,6 +162,8 @@ typedef struct {
     int persistent;           /* 1: the prefill kernel runs persistent CTAs */
     int persistent_ctas;      /* CTAs of the persistent launch (<= SM count) */
     int l2_section_heads;     /* head tiles per L2 section of the persistent tile order */
+    int tile_map;             /* SK_TILE_MAP_GRID or SK_TILE_MAP_PACKED (then grid = (num_ctas, 1, 1)
+                                 and the plan echo lists only the CTAs that have work) */
 } sk_attn_plan_info;
 
 /* Plan only (host, no device work).  Fills *info.  Same argument meaning as

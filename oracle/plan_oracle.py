@@ -176,8 +176,13 @@ def choose_splits(policy: str, B: int, head_tiles: int, num_m_blocks: int, kv_le
 
 def cta_table(sq: int, kv_lens, G: int, pack_gqa: bool, head_tiles: int, block_m: int,
               block_n: int, num_m_blocks: int, num_splits_grid: int, splits_b, causal: bool,
-              window_left: int):
-    """Per-CTA (n_block_min, n_block_max, split word, has_work) in launch order."""
+              window_left: int, packed: bool = False):
+    """Per-CTA (n_block_min, n_block_max, split word, has_work) in launch order.
+
+    packed: the varlen scheduler's launch order (tiling chapter section 4.5, a
+    warp prefix sum over the sequences' tile counts maps each launched CTA to a
+    tile): only the CTAs whose split index is below their sequence's split
+    count are launched, in the same relative order."""
     is_causal, local, wl, wr = mask_flags(causal, window_left)
     reverse = bool(causal) or window_left >= 0
     out = []
@@ -189,7 +194,8 @@ def cta_table(sq: int, kv_lens, G: int, pack_gqa: bool, head_tiles: int, block_m
                 sb = splits_b[b]
                 word = (sb << 16) | split
                 if split >= sb:
-                    out.append((0, 0, word, 0))
+                    if not packed:
+                        out.append((0, 0, word, 0))
                     continue
                 lo, hi = n_block_min_max(sq, kv_lens[b], m_block, block_m, block_n, is_causal,
                                          local, wl, wr, pack_gqa, G, split_word=word)

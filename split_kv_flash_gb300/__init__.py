@@ -19,7 +19,7 @@ __all__ = [
     "SK_PATH_PREFILL", "SK_PATH_LATENT", "SK_PATH_LINEAR_RECURRENT", "SK_PATH_LINEAR_CHUNK", "sk_attn_plan_latent", "sk_attn_fwd_latent", "attn_fwd_latent",
     "LATENT_DQK", "LATENT_DV", "LinearAttnInfo", "sk_linear_attn_plan", "sk_linear_attn_fwd",
     "linear_attn_fwd", "LINEAR_ATTN_DIM", "SK_COMBINE_AUTO", "SK_COMBINE_KERNEL", "SK_COMBINE_IN_KERNEL", "SK_SCHEDULE_AUTO",
-    "SK_SCHEDULE_ONE_TILE", "SK_SCHEDULE_PERSISTENT", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
+    "SK_SCHEDULE_ONE_TILE", "SK_SCHEDULE_PERSISTENT", "SK_TILE_MAP_AUTO", "SK_TILE_MAP_GRID", "SK_TILE_MAP_PACKED", "SK_POLICY_FILL", "SK_POLICY_FA_HEURISTIC", "SK_POLICY_FIXED_CHUNK",
     "SK_POLICY_MIN_CHUNK",
 ]
 
@@ -35,6 +35,7 @@ SK_PATH_LINEAR_RECURRENT, SK_PATH_LINEAR_CHUNK = 4, 5
 LATENT_DQK, LATENT_DV = 576, 512  # latent attention: 512 latent + 64 rotary key columns, 512 value columns
 SK_COMBINE_AUTO, SK_COMBINE_KERNEL, SK_COMBINE_IN_KERNEL = 0, 1, 2
 SK_SCHEDULE_AUTO, SK_SCHEDULE_ONE_TILE, SK_SCHEDULE_PERSISTENT = 0, 1, 2
+SK_TILE_MAP_AUTO, SK_TILE_MAP_GRID, SK_TILE_MAP_PACKED = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 16 << 20  # SK_NOALLOC_SCRATCH_BYTES in include/sk_attn.h
 
 
@@ -47,6 +48,7 @@ class Opts(ctypes.Structure):
         ("debug_inject_stall", ctypes.c_int),
         ("event_begin", ctypes.c_void_p), ("event_end", ctypes.c_void_p),
         ("combine_mode", ctypes.c_int), ("prefill_schedule", ctypes.c_int),
+        ("tile_map", ctypes.c_int),
     ]
 
 
@@ -63,6 +65,7 @@ class PlanInfo(ctypes.Structure):
         ("o_part_offset", ctypes.c_size_t), ("combine_in_kernel", ctypes.c_int),
         ("counter_offset", ctypes.c_size_t), ("persistent", ctypes.c_int),
         ("persistent_ctas", ctypes.c_int), ("l2_section_heads", ctypes.c_int),
+        ("tile_map", ctypes.c_int),
     ]
 
     def as_dict(self):

@@ -163,6 +163,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct CallKey {
     int dev, B, Hq, Hkv, q_len, d, dv, latent, causal, window_left;
     int policy, force_num_splits, force_pack_gqa, force_path, max_splits, num_sms, combine_mode, prefill_schedule;
+    int tile_map;
     const void *q, *k, *v, *out;
 };
 
@@ -306,6 +307,7 @@ sk_status fwd_impl(const void* q, const void* k, const void* v, void* out, float
     key.force_path = o.force_path; key.max_splits = o.max_splits; key.num_sms = o.num_sms;
     key.combine_mode = o.combine_mode;
     key.prefill_schedule = o.prefill_schedule;
+    key.tile_map = o.tile_map;
     key.q = q; key.k = k; key.v = v; key.out = out;
     const CallEntry* ce = kv_len_host ? lookup_call(key, kv_len_host) : nullptr;
     if (!ce) {
@@ -403,6 +405,7 @@ sk_status fwd_impl(const void* q, const void* k, const void* v, void* out, float
     fp.q_tma = q_tma ? 1 : 0;
     fp.q_gp = q_gp;
     fp.o_tma = o_tma ? 1 : 0;
+    fp.packed_grid = p.packed_grid ? 1 : 0;
 
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e;
@@ -593,6 +596,6 @@ const char* sk_attn_status_string(sk_status s) {
 
 const char* sk_attn_last_error(void) { return g_last_error.c_str(); }
 
-int sk_attn_version(void) { return 103; }
+int sk_attn_version(void) { return 104; }
 
 }  // extern "C"

@@ -52,6 +52,7 @@ struct FwdParams {
     int q_gp;          // query heads per row group of that map (G with PackGQA, else 1)
     int o_tma;         // prefill: final O halves leave by TMA through the 5-D O map
     int fused_combine; // decode: the last split CTA of a tile merges the tile's partials
+    int packed_grid;   // decode, varlen: 1-D grid over the CTAs with work (packed_tile_of_cta)
 };
 
 // Per-sequence lengths, offsets and split counts.  Equal lengths need no table.
@@ -70,6 +71,45 @@ struct VarlenSeqs {
     __device__ __forceinline__ int seq_off(int b) const { return off[b]; }
     __device__ __forceinline__ int splits_of(int b) const { return splits[b]; }
 };
+
+// Packed tile map (tiling chapter section 4.5: the varlen scheduler finds a
+// tile's sequence by a warp prefix sum over the sequences' tile counts).  The
+// grid is one-dimensional over the CTAs that have work, in the order of the
+// rectangular grid without its empty CTAs: sequence b owns head_tiles x
+// splits_b x num_m_blocks consecutive CTAs (head tile, then split, then m
+// block fastest).  Called by whole warps; every lane returns the same tile.
+template <class Seqs>
+__device__ __forceinline__ TileCoord packed_tile_of_cta(int cta, const FwdParams& p, const Seqs& seqs) {
+    const int lane = threadIdx.x & 31;
+    const int unit = p.head_tiles * p.num_m_blocks;  // CTAs per split of one sequence
+    const int slot = cta / unit;                      // the CTA's split slot over all sequences
+    const int chunk = (p.B + 31) >> 5;                // sequences per lane
+    const int b0 = min(lane * chunk, p.B), b1 = min(b0 + chunk, p.B);
+    int mine = 0;
+    for (int b = b0; b < b1; ++b) mine += seqs.splits_of(b);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int excl = incl - mine;
+    const unsigned hit = __ballot_sync(0xffffffffu, slot >= excl && slot < incl);
+    const int src = hit ? __ffs(hit) - 1 : 31;
+    int base = __shfl_sync(0xffffffffu, excl, src);
+    int b = min(src * chunk, p.B - 1);
+    while (b < p.B - 1 && base + seqs.splits_of(b) <= slot) base += seqs.splits_of(b++);
+    const int sb = max(seqs.splits_of(b), 1);
+    const int l = cta - base * unit;  // index inside sequence b
+    const int bx = l % p.num_m_blocks;
+    const int rest = l / p.num_m_blocks;
+    TileCoord t;
+    t.m_block = p.reverse_m ? p.num_m_blocks - 1 - bx : bx;
+    t.split = rest % sb;
+    t.head_tile = rest / sb;
+    t.batch = b;
+    return t;
+}
 
 // Packed row r of head tile ht -> (query position i, query head h).
 // Tiling chapter section 6.1/6.3: with PackGQA the G query heads of KV head ht

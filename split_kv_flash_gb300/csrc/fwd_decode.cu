@@ -193,8 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
 
     // ---- which tile
-    const TileCoord tc = tile_of_cta(blockIdx.x, blockIdx.y, blockIdx.z, p.num_m_blocks, p.num_splits,
-                                     p.reverse_m != 0);
+    const TileCoord tc = p.packed_grid ? packed_tile_of_cta(int(blockIdx.x), p, seqs)
+                                       : tile_of_cta(blockIdx.x, blockIdx.y, blockIdx.z, p.num_m_blocks, p.num_splits,
+                                                     p.reverse_m != 0);
     const int b = tc.batch;
     const int ht = tc.head_tile;
     const int sb = seqs.splits_of(b);

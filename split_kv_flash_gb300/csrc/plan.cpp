@@ -212,6 +212,8 @@ sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host
         return fail(SK_ERR_INVALID_ARG, "unknown combine mode");
     if (opts.prefill_schedule < SK_SCHEDULE_AUTO || opts.prefill_schedule > SK_SCHEDULE_PERSISTENT)
         return fail(SK_ERR_INVALID_ARG, "unknown prefill schedule");
+    if (opts.tile_map < SK_TILE_MAP_AUTO || opts.tile_map > SK_TILE_MAP_PACKED)
+        return fail(SK_ERR_INVALID_ARG, "unknown tile map");
 
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.sq = q_len; p.d = d;
     p.dv = dv;
@@ -363,6 +365,21 @@ sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host
     p.grid_z = B;
     if (p.grid_y > 65535) return fail(SK_ERR_UNSUPPORTED, "heads x splits exceeds 65535");
     p.num_ctas = (long long)p.grid_x * p.grid_y * p.grid_z;
+    // Packed tile map (tiling chapter section 4.5, the varlen scheduler): only
+    // the CTAs that have work, in the grid's order; sequence b owns head_tiles x
+    // splits_b x num_m_blocks consecutive CTAs.
+    if (opts.tile_map == SK_TILE_MAP_PACKED && p.path == SK_PATH_DECODE && !latent && B > 1) {
+        long long work = 0;
+        for (int b = 0; b < B; ++b) work += p.splits_b[size_t(b)];
+        work *= (long long)p.head_tiles * p.num_m_blocks;
+        if (work < p.num_ctas && work < (1LL << 31)) {
+            p.packed_grid = true;
+            p.grid_x = int(work);
+            p.grid_y = 1;
+            p.grid_z = 1;
+            p.num_ctas = work;
+        }
+    }
 
     // Workspace: [status header 256 B][plan echo][LSE partials][O partials].
     size_t off = 256;
@@ -389,13 +406,17 @@ sk_status make_plan_ex(int B, int Hq, int Hkv, int q_len, const int* kv_len_host
 
 void plan_ranges(const Plan& p, int32_t* out) {
     long long idx = 0;
-    for (int bz = 0; bz < p.grid_z; ++bz)
-        for (int by = 0; by < p.grid_y; ++by)
-            for (int bx = 0; bx < p.grid_x; ++bx, ++idx) {
+    const int gy = p.packed_grid ? p.head_tiles * p.num_splits : p.grid_y;
+    const int gz = p.packed_grid ? p.B : p.grid_z;
+    const int gx = p.packed_grid ? p.num_m_blocks : p.grid_x;
+    for (int bz = 0; bz < gz; ++bz)
+        for (int by = 0; by < gy; ++by)
+            for (int bx = 0; bx < gx; ++bx) {
                 const TileCoord t = tile_of_cta(bx, by, bz, p.num_m_blocks, p.num_splits, p.reverse_m);
                 const int sb = p.splits_b[size_t(t.batch)];
+                if (p.packed_grid && t.split >= sb) continue;  // the packed grid has no such CTA
                 const uint32_t word = split_word(t.split, sb);
-                int32_t* e = out + idx * 4;
+                int32_t* e = out + (idx++) * 4;
                 if (t.split >= sb) {
                     e[0] = 0; e[1] = 0; e[2] = int32_t(word); e[3] = 0;
                     continue;
@@ -433,6 +454,7 @@ void plan_to_info(const Plan& p, sk_attn_plan_info* info) {
     info->persistent = p.persistent ? 1 : 0;
     info->persistent_ctas = p.persistent_ctas;
     info->l2_section_heads = p.l2_section;
+    info->tile_map = p.packed_grid ? SK_TILE_MAP_PACKED : SK_TILE_MAP_GRID;
 }
 
 }  // namespace sk

@@ -60,6 +60,7 @@ struct Plan {
     int persistent_ctas = 0;
     int l2_section = 1;          // head tiles per L2 section of the persistent tile order
     bool reverse_m = false;
+    bool packed_grid = false;    // decode, varlen: 1-D grid over the CTAs with work (tiling chapter 4.5)
     int grid_x = 0, grid_y = 0, grid_z = 0;
     long long num_ctas = 0;
     int num_sms = 0;

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(sk):
 
 
 def test_version_and_status_strings(sk):
-    assert sk.sk_attn_version() == 103
+    assert sk.sk_attn_version() == 104
     assert sk.sk_attn_status_string(0) == "SK_OK"
     assert sk.sk_attn_status_string(6) == "SK_ERR_DEVICE_TIMEOUT"
     assert sk.sk_attn_status_string(99) == "SK_ERR_UNKNOWN"
@@ -146,7 +146,7 @@ def test_combine_mode_in_plan(sk):
     with pytest.raises(sk.SKError) as ei:
         sk.sk_attn_plan(1, 32, 4, 1, [4096], 128, opts=_opts(sk, combine_mode=5))
     assert ei.value.status == 1
-    assert sk.sk_attn_version() == 103
+    assert sk.sk_attn_version() == 104
 
 
 def test_persistent_prefill_plan(sk):

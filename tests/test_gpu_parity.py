@@ -65,6 +65,21 @@ def test_varlen_decode_large(sk, B):
     _check_full(sk, wl.varlen_decode(B))
 
 
+@pytest.mark.parametrize("combine", [0, 2])
+@pytest.mark.parametrize("B", [2, 8, 32])
+def test_varlen_decode_packed_tile_map(sk, B, combine):
+    """The packed tile map (one-dimensional grid over the CTAs with work, each
+    finding its sequence by a warp prefix sum), with the combine kernel and with
+    the in-kernel merge: same results as the oracle."""
+    o = sk.Opts()
+    o.tile_map = sk.SK_TILE_MAP_PACKED
+    o.combine_mode = combine
+    w = wl.varlen_decode(B)
+    info = sk.sk_attn_plan(w.B, w.Hq, w.Hkv, w.q_len, w.kv_len, w.d, w.causal, w.window_left, o)
+    assert info.tile_map == sk.SK_TILE_MAP_PACKED
+    _check_full(sk, w, opts=o, tag=w.name + "_packed")
+
+
 @pytest.mark.parametrize("local", [False, True])
 def test_prefill_8192(sk, local):
     """Sampled rows over every head, plus one whole head of every sequence: all

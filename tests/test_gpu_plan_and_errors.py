@@ -26,6 +26,8 @@ ECHO_CASES = [
     ("prefill_local", 2, 8, 2, 128, 1024, [1024, 1024], True, 200, 0),
     ("prefill_split", 1, 4, 2, 128, 300, [4000], True, -1, 3),
     ("fa_policy", 1, 32, 4, 128, 1, [65536], False, -1, -2),
+    ("varlen_packed", 8, 32, 8, 128, 1, wl.varlen_lengths(8, 1303), False, -1, -3),
+    ("varlen_packed_many", 37, 8, 2, 64, 1, wl.varlen_lengths(37, 1304), False, -1, -3),
 ]
 
 
@@ -39,6 +41,8 @@ def test_plan_echo_bit_exact(sk, case):
         opts.force_num_splits = force
     if force == -2:
         opts.policy = sk.SK_POLICY_FA_HEURISTIC
+    if force == -3:
+        opts.tile_map = sk.SK_TILE_MAP_PACKED
     q, k, v = wl.make_inputs(w)
     qg, kg, vg = H.to_gpu(q, k, v)
     out, lse, ws = sk.attn_fwd(qg, kg, vg, kv, w.scale, causal, window, opts=opts)
@@ -46,6 +50,8 @@ def test_plan_echo_bit_exact(sk, case):
     echo = sk.sk_attn_read_plan_echo(ws, info.num_ctas)
     host = sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, opts)
     assert np.array_equal(np.array(echo, dtype=np.int32), np.array(host, dtype=np.int32))
+    if force == -3:
+        assert info.tile_map == sk.SK_TILE_MAP_PACKED and info.grid_y == 1 and info.grid_z == 1
 
 
 def test_outputs_stay_in_bounds(sk):

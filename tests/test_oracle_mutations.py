@@ -114,6 +114,7 @@ PLAN_MUTATIONS = {
                                   "m_idx_max = m_idx_max"),
     "local_lower_bound_dropped": ("n_block_min = max(0, c_div(n_idx_left, block_n))", "n_block_min = 0"),
     "block_offset_dropped": ("n_idx = m_idx_max + seqlen_k - seqlen_q", "n_idx = m_idx_max"),
+    "packed_keeps_empty_ctas": ("                    if not packed:\n", "                    if True:\n"),
     "heuristic_threshold_080": (">= 0.85 * float(best)", ">= 0.8 * float(best)"),
     "l2_budget_32mb": ("L2_SPLIT_BYTES = 50 * 1024 * 1024", "L2_SPLIT_BYTES = 32 * 1024 * 1024"),
     "split_share_floor": ("per = ceil_div(n_block_max - n_block_min, n_split)",

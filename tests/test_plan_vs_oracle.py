@@ -257,3 +257,40 @@ def test_product_ranges_match_brute_force_visibility(sk):
             if need:
                 share = -(-len(need) // ns)
                 assert all(table[s * nm + bx][1] - table[s * nm + bx][0] <= share for s in range(ns))
+
+
+def test_packed_tile_map_matches_oracle(sk):
+    """The packed tile map (tiling chapter section 4.5): on the decode path,
+    when sequences of one batch have different split counts, the grid is one
+    dimension over exactly the CTAs with work, in the oracle's packed launch
+    order; everywhere else the option leaves the rectangular grid."""
+    packed_seen = 0
+    for num_sms in (148, 152):
+        for (B, Hq, Hkv, sq, kv, d, causal, window) in _cases():
+            o = _opts(sk, 0, num_sms, tile_map=sk.SK_TILE_MAP_PACKED)
+            info = sk.sk_attn_plan(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            sb = po.split_counts(kv, 128, info.num_splits_policy)
+            work = sum(sb) * info.head_tiles * info.num_m_blocks
+            grid = info.head_tiles * info.num_splits * info.num_m_blocks * B
+            packed = info.path == sk.SK_PATH_DECODE and B > 1 and work < grid
+            assert info.tile_map == (sk.SK_TILE_MAP_PACKED if packed else sk.SK_TILE_MAP_GRID)
+            exp = po.cta_table(sq, kv, Hq // Hkv, bool(info.pack_gqa), info.head_tiles, info.kBlockM, 128,
+                               info.num_m_blocks, info.num_splits, sb, causal, window, packed=packed)
+            got = sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, o)
+            assert same_table(got, exp), (B, Hq, Hkv, sq, kv, d, causal, window, num_sms)
+            if packed:
+                packed_seen += 1
+                assert (info.grid_x, info.grid_y, info.grid_z) == (work, 1, 1)
+                assert info.num_ctas == work
+                # the same problem without the option: the grid, and the same tiles
+                g = sk.sk_attn_plan(B, Hq, Hkv, sq, kv, d, causal, window, _opts(sk, 0, num_sms))
+                assert g.tile_map == sk.SK_TILE_MAP_GRID and g.num_ctas == grid
+                full = sk.sk_attn_plan_ranges(B, Hq, Hkv, sq, kv, d, causal, window, _opts(sk, 0, num_sms))
+                assert [list(r) for r in full if r[3]] == [list(r) for r in got]
+    assert packed_seen >= 10
+
+
+def test_unknown_tile_map_is_rejected(sk):
+    with pytest.raises(sk.SKError) as ei:
+        sk.sk_attn_plan(2, 8, 2, 1, [100, 5000], 128, False, -1, _opts(sk, tile_map=3))
+    assert ei.value.status == 1
